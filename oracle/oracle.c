@@ -1,0 +1,285 @@
+/*
+ * oracle.c -- plain, slow, CPU reference for the paged key scoring and the
+ * exact top-k selection of a sparse-attention decode step.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  The GPU library never
+ * includes, links or calls it, and this file includes nothing from it.
+ *
+ * What it follows:
+ *  - The score is the indexer's: for query row r and key position j
+ *        s[r,j] = sum_h w[r,h] * ReLU( q[r,h,:] . (k[j,:] * scale[j]) )
+ *    with k stored as FP8 E4M3 and one f32 scale per key.  The reference check
+ *    of "sgl-amd-mono-upstream PR 18" (GLM-5.3 indexer launch), section
+ *    "Modifications / 0. An exact top-k check", recomputes launch scores in
+ *    f64 from the launch's own bf16 query, head weights and cached keys; this
+ *    file does the same, literally, in double precision.
+ *  - The selection list: the keys strictly above the k-th largest score in
+ *    ascending position, then the keys tied with it in ascending position
+ *    until the list holds k; rows with n <= k keep every key and pad with -1.
+ *    The same page's "missed" count defines the exact top-k set as the first
+ *    k keys by (score descending, position ascending); the list here is built
+ *    from that set by a full sort.
+ *
+ * Nothing here is blocked, fused or reordered beyond the definitions above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- formats */
+
+/* FP8 E4M3 (the OCP "fn" variant used by FP8 KV caches): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits.  Exponent field 0 holds the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no infinities, so the
+ * largest finite value is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_f64(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* bf16 is the upper half of an IEEE-754 binary32. */
+double oracle_bf16_to_f64(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ReLU that lets NaN through (a NaN dot product must not turn into 0). */
+static double relu(double x)
+{
+    if (isnan(x))
+        return x;
+    return x > 0.0 ? x : 0.0;
+}
+
+/* ------------------------------------------------------------------ scores */
+
+/* Error codes shared by the entry points below. */
+enum { OR_OK = 0, OR_ERR_ARG = -1, OR_ERR_BOUNDS = -6 };
+
+typedef struct {
+    int q_is_e4m3;               /* 0: q holds bf16 bits, 1: q holds E4M3 codes */
+    const void *q;               /* [R][H][D] */
+    const float *head_w;         /* [R][H] */
+    const uint8_t *k_cache;      /* [pool_pages][P][D] E4M3 codes */
+    const float *k_scale;        /* [pool_pages][P] */
+    int64_t pool_pages;
+    const int32_t *block_table;  /* [n_req][max_pages] */
+    int max_pages;
+    const int32_t *seq_lens;     /* [R] keys visible to each row */
+    const int32_t *row_req;      /* [R] request of each row */
+    int R, H, D, P;
+} oracle_problem;
+
+static double q_value(const oracle_problem *pb, int r, int h, int d)
+{
+    size_t i = ((size_t)r * pb->H + h) * pb->D + d;
+    if (pb->q_is_e4m3)
+        return oracle_e4m3_to_f64(((const uint8_t *)pb->q)[i]);
+    return oracle_bf16_to_f64(((const uint16_t *)pb->q)[i]);
+}
+
+/* s[r, j] by the literal formula.  Key j of row r lives in page
+ * block_table[row_req[r]][j / P], slot j % P. */
+static int score_one(const oracle_problem *pb, int r, int64_t j, double *out)
+{
+    int req = pb->row_req[r];
+    int64_t page_idx = j / pb->P;
+    int slot = (int)(j % pb->P);
+    int32_t page;
+    double *kf;
+    double s = 0.0;
+    int h, d;
+
+    if (j < 0 || j >= pb->seq_lens[r] || page_idx >= pb->max_pages)
+        return OR_ERR_BOUNDS;
+    page = pb->block_table[(int64_t)req * pb->max_pages + page_idx];
+    if (page < 0 || page >= pb->pool_pages)
+        return OR_ERR_BOUNDS;
+
+    /* k[j,:] * scale[j], each element decoded from its E4M3 code. */
+    kf = (double *)malloc(sizeof(double) * (size_t)pb->D);
+    if (!kf)
+        return OR_ERR_ARG;
+    for (d = 0; d < pb->D; ++d) {
+        size_t ki = ((size_t)page * pb->P + slot) * pb->D + d;
+        kf[d] = oracle_e4m3_to_f64(pb->k_cache[ki]) *
+                (double)pb->k_scale[(size_t)page * pb->P + slot];
+    }
+    for (h = 0; h < pb->H; ++h) {
+        double dot = 0.0;
+        for (d = 0; d < pb->D; ++d)
+            dot += q_value(pb, r, h, d) * kf[d];
+        s += (double)pb->head_w[(size_t)r * pb->H + h] * relu(dot);
+    }
+    free(kf);
+    *out = s;
+    return OR_OK;
+}
+
+static int check_problem(const oracle_problem *pb)
+{
+    int r;
+    if (!pb->q || !pb->head_w || !pb->k_cache || !pb->k_scale || !pb->block_table ||
+        !pb->seq_lens || !pb->row_req)
+        return OR_ERR_ARG;
+    if (pb->R < 0 || pb->H <= 0 || pb->D <= 0 || pb->P <= 0 || pb->max_pages < 0)
+        return OR_ERR_ARG;
+    for (r = 0; r < pb->R; ++r) {
+        if (pb->seq_lens[r] < 0 || (int64_t)pb->seq_lens[r] > (int64_t)pb->max_pages * pb->P)
+            return OR_ERR_BOUNDS;
+        if (pb->row_req[r] < 0)
+            return OR_ERR_ARG;
+    }
+    return OR_OK;
+}
+
+/* Every score of every row: out[r * out_stride + j] for j < seq_lens[r].
+ * Entries at j >= seq_lens[r] are not written. */
+int oracle_scores(int q_is_e4m3, const void *q, const float *head_w,
+                  const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                  const int32_t *block_table, int max_pages,
+                  const int32_t *seq_lens, const int32_t *row_req,
+                  int R, int H, int D, int P, double *out, int64_t out_stride)
+{
+    oracle_problem pb = {q_is_e4m3, q, head_w, k_cache, k_scale, pool_pages,
+                         block_table, max_pages, seq_lens, row_req, R, H, D, P};
+    int r, st = check_problem(&pb);
+    if (st != OR_OK)
+        return st;
+    for (r = 0; r < R; ++r) {
+        int64_t j;
+        if ((int64_t)seq_lens[r] > out_stride)
+            return OR_ERR_ARG;
+        for (j = 0; j < seq_lens[r]; ++j) {
+            st = score_one(&pb, r, j, &out[(int64_t)r * out_stride + j]);
+            if (st != OR_OK)
+                return st;
+        }
+    }
+    return OR_OK;
+}
+
+/* The scores of one row at the listed positions only (for sampled checks of
+ * workloads too large to score whole on the CPU). */
+int oracle_score_positions(int q_is_e4m3, const void *q, const float *head_w,
+                           const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                           const int32_t *block_table, int max_pages,
+                           const int32_t *seq_lens, const int32_t *row_req,
+                           int R, int H, int D, int P,
+                           int row, const int64_t *positions, int64_t npos, double *out)
+{
+    oracle_problem pb = {q_is_e4m3, q, head_w, k_cache, k_scale, pool_pages,
+                         block_table, max_pages, seq_lens, row_req, R, H, D, P};
+    int64_t i;
+    int st = check_problem(&pb);
+    if (st != OR_OK)
+        return st;
+    if (row < 0 || row >= R)
+        return OR_ERR_ARG;
+    for (i = 0; i < npos; ++i) {
+        st = score_one(&pb, row, positions[i], &out[i]);
+        if (st != OR_OK)
+            return st;
+    }
+    return OR_OK;
+}
+
+/* --------------------------------------------------------------- selection */
+
+/* Ranking of f32 scores: larger first; every NaN ranks below every number and
+ * all NaNs tie; -0 and +0 tie (plain float comparison). */
+static int ranks_above(float a, float b)
+{
+    if (isnan(a))
+        return 0;
+    if (isnan(b))
+        return 1;
+    return a > b;
+}
+
+static int ties_with(float a, float b)
+{
+    if (isnan(a) || isnan(b))
+        return isnan(a) && isnan(b);
+    return a == b;
+}
+
+typedef struct {
+    float s;
+    int32_t pos;
+} scored_pos;
+
+/* Score descending, then position ascending: a total order on distinct
+ * positions, so the sort result does not depend on qsort's stability. */
+static int cmp_desc_then_pos(const void *pa, const void *pb)
+{
+    const scored_pos *a = (const scored_pos *)pa, *b = (const scored_pos *)pb;
+    if (ranks_above(a->s, b->s))
+        return -1;
+    if (ranks_above(b->s, a->s))
+        return 1;
+    return (a->pos > b->pos) - (a->pos < b->pos);
+}
+
+/* Exact top-k list of one row of n scores (see the header comment). */
+int oracle_topk(const float *scores, int64_t n, int k, int32_t *out)
+{
+    scored_pos *v;
+    float t;
+    int64_t j;
+    int filled = 0;
+
+    if (k <= 0 || n < 0 || (n > 0 && !scores) || !out)
+        return OR_ERR_ARG;
+    if (n <= k) {
+        for (j = 0; j < k; ++j)
+            out[j] = j < n ? (int32_t)j : -1;
+        return OR_OK;
+    }
+    v = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+    if (!v)
+        return OR_ERR_ARG;
+    for (j = 0; j < n; ++j) {
+        v[j].s = scores[j];
+        v[j].pos = (int32_t)j;
+    }
+    qsort(v, (size_t)n, sizeof(scored_pos), cmp_desc_then_pos);
+    t = v[k - 1].s; /* the k-th largest score, counting repeats */
+    free(v);
+
+    for (j = 0; j < n && filled < k; ++j)
+        if (ranks_above(scores[j], t))
+            out[filled++] = (int32_t)j;
+    for (j = 0; j < n && filled < k; ++j)
+        if (ties_with(scores[j], t))
+            out[filled++] = (int32_t)j;
+    return filled == k ? OR_OK : OR_ERR_ARG;
+}
+
+/* Many rows at once: row r has n = lens[r] scores at scores + r*stride. */
+int oracle_topk_rows(const float *scores, int64_t stride, const int32_t *lens, int R,
+                     int k, int32_t *out)
+{
+    int r, st;
+    for (r = 0; r < R; ++r) {
+        st = oracle_topk(scores + (int64_t)r * stride, lens[r], k, out + (int64_t)r * k);
+        if (st != OR_OK)
+            return st;
+    }
+    return OR_OK;
+}
