@@ -1,0 +1,157 @@
+/*
+ * idx.h -- C ABI of the GB300 index chain: paged FP8 key scoring and exact
+ * top-k selection for sparse-attention decode.
+ *
+ * The operation is the one of "sgl-amd-mono-upstream PR 18" (GLM-5.3 indexer
+ * launch): section "Modifications / 2. A request's rows scored together"
+ * (every row of a request scores that request's paged index keys in one pass,
+ * each key read once) and section "Modifications / 3. Every row's exact
+ * top-2048 on up to 64 slices" (radix select with all-gathered digit
+ * histograms).  The score is the indexer's
+ *
+ *     s[r, j] = sum_h w[r, h] * ReLU( q[r, h, :] . (k[j, :] * scale[j]) )
+ *
+ * with k an FP8 E4M3 key, scale its f32 per-key scale, q a bf16 (or E4M3)
+ * query row of H = 64 heads of D = 128 dims, accumulated in f32.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no pointer after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; no entry point synchronises except
+ *    idx_check_status.
+ *  - A returned idx_status reports argument errors found on the host before
+ *    anything is enqueued (nothing is launched then) and launch errors.
+ *    Errors found by the kernels (a block-table entry outside the pool, a row
+ *    longer than its block table, a wait that timed out) are OR-ed into a
+ *    status word in the workspace and read with idx_check_status.
+ *  - Shapes are fixed: IDX_HEADS heads, IDX_DIM dims, IDX_PAGE tokens a page.
+ */
+#ifndef IDX_H
+#define IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_HEADS 64      /* index heads per query row */
+#define IDX_DIM 128       /* index head dimension */
+#define IDX_PAGE 64       /* tokens per key-cache page */
+#define IDX_MAX_K 2048    /* largest k of the top-k */
+#define IDX_MAX_ROWS 1024 /* most query rows in one call */
+#define IDX_GROUP_ROWS 4  /* rows of one request scored in one pass */
+
+typedef enum {
+    IDX_OK = 0,
+    IDX_ERR_ARG = -1,       /* a NULL pointer, a size out of range */
+    IDX_ERR_ALIGN = -2,     /* a pointer or stride that breaks the alignment rule */
+    IDX_ERR_WORKSPACE = -3, /* workspace NULL or smaller than idx_workspace_bytes */
+    IDX_ERR_CUDA = -4,      /* a CUDA call failed (launch, attribute, ...) */
+    IDX_ERR_TIMEOUT = -5,   /* device: a bounded wait gave up */
+    IDX_ERR_BOUNDS = -6,    /* device: block-table id outside the pool, or a row
+                               longer than its block table (row treated as shorter) */
+    IDX_ERR_UNSUPPORTED = -7 /* no sm_103a device, or a missing driver feature */
+} idx_status;
+
+typedef enum {
+    IDX_Q_BF16 = 0, /* q holds bf16 values */
+    IDX_Q_E4M3 = 1  /* q holds FP8 E4M3 codes; any per-(row, head) scale of q
+                       is the caller's to fold into head_w */
+} idx_qtype;
+
+/* Bytes of workspace the calls below need for R rows, rows of at most
+ * `max_len` keys and top-k size k.  `with_scores` != 0 adds room for an f32
+ * score matrix [R][round_up(max_len, 4)], used by idx_score_topk when the
+ * caller passes scores == NULL.  The workspace must be 256-byte aligned and
+ * zeroed once before its first use (idx_workspace_init does that). */
+size_t idx_workspace_bytes(int R, int64_t max_len, int k, int with_scores);
+
+/* Zero the workspace's status word (asynchronously on `stream`). */
+idx_status idx_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * idx_score -- score every key of each row's request against the row.
+ *
+ *  qtype        IDX_Q_BF16 or IDX_Q_E4M3
+ *  q            [R][IDX_HEADS][IDX_DIM] bf16 or E4M3, 16-byte aligned
+ *  head_w       [R][IDX_HEADS] f32
+ *  k_cache      [pool_pages][IDX_PAGE][IDX_DIM] E4M3 codes, 16-byte aligned
+ *  k_scale      [pool_pages][IDX_PAGE] f32, 16-byte aligned; every scale >= 0
+ *               (the scale is taken out of the ReLU)
+ *  pool_pages   pages in the pool (1 .. 2^25)
+ *  block_table  [n_req][max_pages] int32: page ids of request i's keys in
+ *               position order (key j of a request is page j/64, slot j%64)
+ *  max_pages    row stride of block_table
+ *  seq_lens     [R] int32: keys visible to row r (its request's first seq_lens[r])
+ *  row_req      [R] int32: request of row r.  Consecutive rows of one request
+ *               are scored together, IDX_GROUP_ROWS at a time.
+ *  scores       [R][score_stride] f32 out: scores[r][j] for j < seq_lens[r];
+ *               entries at j >= seq_lens[r] are left untouched.  -0 is written
+ *               as +0.  16-byte aligned, score_stride a multiple of 4 and at
+ *               least the longest row.
+ *  workspace    >= idx_workspace_bytes(R, score_stride, 1, 0) bytes
+ *
+ * Errors: IDX_ERR_ARG (NULL pointer, R outside [1, IDX_MAX_ROWS], bad sizes),
+ * IDX_ERR_ALIGN, IDX_ERR_WORKSPACE, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA.
+ */
+idx_status idx_score(int qtype, const void *q, const float *head_w,
+                     const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                     const int32_t *block_table, int max_pages,
+                     const int32_t *seq_lens, const int32_t *row_req, int R,
+                     float *scores, int64_t score_stride,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * idx_topk -- exact top-k list of each row of a score matrix.
+ *
+ * The list of row r (n = row_lens[r] scores) holds the positions whose score
+ * is strictly above the k-th largest score, in ascending position, then the
+ * positions whose score equals it, in ascending position, until k entries.
+ * Rows with n <= k list 0..n-1 and pad with -1.  Scores compare as f32 with
+ * -0 == +0; a NaN ranks below every number (finite inputs are expected).
+ *
+ *  scores       [R][score_stride] f32, 16-byte aligned, score_stride % 4 == 0
+ *  row_lens     [R] int32, each in [0, score_stride]
+ *  k            1 .. IDX_MAX_K
+ *  indices      [R][k] int32 out
+ *  workspace    status word holder (>= idx_workspace_bytes(R, score_stride, k, 0)
+ *               bytes); may be NULL, then device errors are not reported
+ *
+ * Errors: IDX_ERR_ARG, IDX_ERR_ALIGN, IDX_ERR_WORKSPACE, IDX_ERR_CUDA.
+ */
+idx_status idx_topk(const float *scores, int64_t score_stride, const int32_t *row_lens,
+                    int R, int k, int32_t *indices,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * idx_score_topk -- idx_score then idx_topk on the same stream, with no host
+ * round trip in between.  scores may be NULL: the scores then live in the
+ * workspace (size it with with_scores = 1) and score_stride is ignored.
+ * max_len bounds the longest row (used for the launch shape and workspace).
+ */
+idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
+                          const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                          const int32_t *block_table, int max_pages,
+                          const int32_t *seq_lens, const int32_t *row_req, int R,
+                          int64_t max_len, int k, int32_t *indices,
+                          float *scores, int64_t score_stride,
+                          void *workspace, size_t ws_bytes, void *stream);
+
+/* Wait for `stream`, read and clear the workspace status word, and return the
+ * first device error recorded since the last call (IDX_OK if none). */
+idx_status idx_check_status(void *workspace, void *stream);
+
+/* A short English name for a status code. */
+const char *idx_status_str(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H */

@@ -1,0 +1,185 @@
+"""ctypes binding of libidx.so (include/idx.h), for torch CUDA tensors.
+
+Argument marshalling only: every function checks dtypes, devices and shapes,
+passes raw device pointers and the current CUDA stream, and turns a non-zero
+status into an exception.  All computation happens in the library's kernels;
+there is no CPU fallback, and loading fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+HEADS, DIM, PAGE, MAX_K, MAX_ROWS, GROUP_ROWS = 64, 128, 64, 2048, 1024, 4
+Q_BF16, Q_E4M3 = 0, 1
+OK = 0
+STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORKSPACE",
+          -4: "IDX_ERR_CUDA", -5: "IDX_ERR_TIMEOUT", -6: "IDX_ERR_BOUNDS", -7: "IDX_ERR_UNSUPPORTED"}
+
+EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
+           "idx_check_status", "idx_status_str", "idx_version")
+
+_lib = None
+
+
+class IdxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (where, STATUS.get(status, "?"), status))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libidx.so (optionally building it first). Raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError("libidx.so is not built (%s); run key_scoring_exact_gb300.build.build()" % path)
+        _build.build()
+    lib = ctypes.CDLL(path)
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.idx_workspace_bytes.restype = sz
+    lib.idx_workspace_bytes.argtypes = [i32, i64, i32, i32]
+    lib.idx_workspace_init.restype = i32
+    lib.idx_workspace_init.argtypes = [p, sz, p]
+    score_common = [i32, p, p, p, p, i64, p, i32, p, p, i32]
+    lib.idx_score.restype = i32
+    lib.idx_score.argtypes = score_common + [p, i64, p, sz, p]
+    lib.idx_topk.restype = i32
+    lib.idx_topk.argtypes = [p, i64, p, i32, i32, p, p, sz, p]
+    lib.idx_score_topk.restype = i32
+    lib.idx_score_topk.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
+    lib.idx_check_status.restype = i32
+    lib.idx_check_status.argtypes = [p, p]
+    lib.idx_status_str.restype = ctypes.c_char_p
+    lib.idx_status_str.argtypes = [i32]
+    lib.idx_version.restype = i32
+    lib.idx_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError("%s has dtype %s" % (name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _check(st: int, where: str) -> None:
+    if st != OK:
+        raise IdxError(st, where)
+
+
+def workspace_bytes(R: int, max_len: int, k: int = MAX_K, with_scores: bool = False) -> int:
+    return int(load().idx_workspace_bytes(int(R), int(max_len), int(k), 1 if with_scores else 0))
+
+
+def new_workspace(R: int, max_len: int, k: int = MAX_K, with_scores: bool = False,
+                  device=None, stream=None) -> torch.Tensor:
+    """A zero-initialised, 1024-byte aligned workspace tensor (allocated by torch)."""
+    n = workspace_bytes(R, max_len, k, with_scores)
+    if n == 0:
+        raise ValueError("invalid workspace request")
+    raw = torch.zeros(n + 1024, dtype=torch.uint8, device=device or "cuda")
+    off = (-raw.data_ptr()) % 1024
+    ws = raw[off:off + n]
+    _check(load().idx_workspace_init(ws.data_ptr(), n, _stream(stream)), "idx_workspace_init")
+    return ws
+
+
+def _qtype(q: torch.Tensor) -> int:
+    if q.dtype == torch.bfloat16:
+        return Q_BF16
+    if q.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return Q_E4M3
+    raise ValueError("q must be bfloat16 or E4M3 (uint8 / float8_e4m3fn)")
+
+
+def _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req):
+    R = q.shape[0]
+    if tuple(q.shape) != (R, HEADS, DIM) or tuple(head_w.shape) != (R, HEADS):
+        raise ValueError("q must be [R, 64, 128] and head_w [R, 64]")
+    if k_cache.dim() != 3 or tuple(k_cache.shape[1:]) != (PAGE, DIM):
+        raise ValueError("k_cache must be [pool_pages, 64, 128]")
+    if tuple(k_scale.shape) != tuple(k_cache.shape[:2]):
+        raise ValueError("k_scale must be [pool_pages, 64]")
+    if block_table.dim() != 2 or seq_lens.shape != (R,) or row_req.shape != (R,):
+        raise ValueError("block_table [n_req, max_pages], seq_lens [R], row_req [R]")
+    return [_qtype(q), _dev(q, "q"), _dev(head_w, "head_w", torch.float32),
+            _dev(k_cache, "k_cache", (torch.uint8, torch.float8_e4m3fn)),
+            _dev(k_scale, "k_scale", torch.float32), int(k_cache.shape[0]),
+            _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+            _dev(seq_lens, "seq_lens", torch.int32), _dev(row_req, "row_req", torch.int32), int(R)]
+
+
+def score(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, workspace, stream=None):
+    """idx_score: scores[r, j] for j < seq_lens[r] (f32 [R, stride], stride % 4 == 0)."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
+    if scores.dim() != 2 or scores.shape[0] != q.shape[0]:
+        raise ValueError("scores must be [R, stride]")
+    st = load().idx_score(*args, _dev(scores, "scores", torch.float32), int(scores.shape[1]),
+                          _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "idx_score")
+
+
+def topk(scores, row_lens, k, indices, workspace=None, stream=None):
+    """idx_topk: indices[r] = exact top-k list of scores[r, :row_lens[r]]."""
+    R = scores.shape[0]
+    if indices.shape != (R, k):
+        raise ValueError("indices must be [R, k]")
+    ws = _dev(workspace, "workspace", torch.uint8) if workspace is not None else None
+    st = load().idx_topk(_dev(scores, "scores", torch.float32), int(scores.shape[1]),
+                         _dev(row_lens, "row_lens", torch.int32), int(R), int(k),
+                         _dev(indices, "indices", torch.int32), ws,
+                         workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(st, "idx_topk")
+
+
+def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
+               workspace, scores=None, stream=None):
+    """idx_score_topk: scoring then selection on one stream.  With scores=None
+    the scores live in the workspace (size it with with_scores=True)."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
+    if indices.shape != (q.shape[0], k):
+        raise ValueError("indices must be [R, k]")
+    sp = _dev(scores, "scores", torch.float32) if scores is not None else None
+    stride = int(scores.shape[1]) if scores is not None else 0
+    st = load().idx_score_topk(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
+                               stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                               _stream(stream))
+    _check(st, "idx_score_topk")
+
+
+def check_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status."""
+    return int(load().idx_check_status(_dev(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def scores_view(workspace: torch.Tensor, R: int, max_len: int) -> torch.Tensor:
+    """The [R, stride] f32 score matrix that idx_score_topk keeps in the
+    workspace when called with scores=None (layout of idx_workspace_bytes)."""
+    lib = load()
+    no_scores = int(lib.idx_workspace_bytes(int(R), int(max_len), 1, 0))
+    stride = max(4, (int(max_len) + 3) // 4 * 4)
+    n = R * stride
+    return workspace[no_scores:no_scores + 4 * n].view(torch.float32).view(R, stride)

@@ -1,0 +1,236 @@
+// idx_api.cu -- the C ABI declared in include/idx.h: host-side argument
+// checks, workspace layout, TMA descriptors and the launch sequence.
+// No entry point allocates device memory or synchronises (except
+// idx_check_status); all work goes to the caller's stream.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "idx_internal.h"
+
+namespace idx {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int ok = 0;  // sm_103
+    int num_sms = 0;
+};
+
+idx_status device_info(DeviceInfo* out) {
+    static DeviceInfo cache[64];
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64) return IDX_ERR_UNSUPPORTED;
+    if (!cached[dev]) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return IDX_ERR_CUDA;
+        }
+        cache[dev].ok = (major == 10 && minor == 3);
+        cache[dev].num_sms = sms;
+        cached[dev] = 1;
+    }
+    *out = cache[dev];
+    return out->ok ? IDX_OK : IDX_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2D uint8 tensor map: rows of 128 bytes, boxes of 64 rows, 128-byte swizzle.
+idx_status make_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return IDX_ERR_UNSUPPORTED;
+    const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDim};
+    const cuuint32_t box[2] = {(cuuint32_t)kDim, (cuuint32_t)kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
+}
+
+idx_status check_score_args(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                            const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                            int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                            void* workspace) {
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (!q || !head_w || !k_cache || !k_scale || !block_table || !seq_lens || !row_req) return IDX_ERR_ARG;
+    if (R < 1 || R > kMaxRows) return IDX_ERR_ARG;
+    if (pool_pages < 1 || pool_pages > (int64_t(1) << 25)) return IDX_ERR_ARG;
+    if (max_pages < 1 || (int64_t)max_pages * kPage > INT32_MAX) return IDX_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(k_scale, 16)) return IDX_ERR_ALIGN;
+    if (!workspace) return IDX_ERR_WORKSPACE;
+    if (!aligned(workspace, 1024)) return IDX_ERR_ALIGN;
+    return IDX_OK;
+}
+
+idx_status to_status(cudaError_t e) {
+    if (e == cudaSuccess) return IDX_OK;
+    (void)cudaGetLastError();
+    return IDX_ERR_CUDA;
+}
+
+idx_status run_score(const ScoreArgs& a) {
+    CUtensorMap keys_map, q_map;
+    idx_status st = make_rows_map(&keys_map, a.k_cache, (uint64_t)a.pool_pages * kPage);
+    if (st != IDX_OK) return st;
+    st = make_rows_map(&q_map, a.ws + a.L.q8, (uint64_t)2 * a.R * kHeads);
+    if (st != IDX_OK) return st;
+    st = to_status(launch_prep(a));
+    if (st != IDX_OK) return st;
+    return to_status(launch_score(a, keys_map, q_map));
+}
+
+}  // namespace
+}  // namespace idx
+
+using namespace idx;
+
+extern "C" {
+
+size_t idx_workspace_bytes(int R, int64_t max_len, int k, int with_scores) {
+    (void)k;
+    if (R < 1 || R > kMaxRows || max_len < 0) return 0;
+    return ws_layout(R, max_len, with_scores).end;
+}
+
+idx_status idx_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+    if (!workspace || ws_bytes < 256) return IDX_ERR_WORKSPACE;
+    return to_status(cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+idx_status idx_score(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                     const float* k_scale, int64_t pool_pages, const int32_t* block_table, int max_pages,
+                     const int32_t* seq_lens, const int32_t* row_req, int R, float* scores,
+                     int64_t score_stride, void* workspace, size_t ws_bytes, void* stream) {
+    idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
+                                     seq_lens, row_req, R, workspace);
+    if (st != IDX_OK) return st;
+    if (!scores) return IDX_ERR_ARG;
+    if (score_stride < 4 || score_stride % 4 != 0) return IDX_ERR_ALIGN;
+    if (!aligned(scores, 16)) return IDX_ERR_ALIGN;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    const WsLayout L = ws_layout(R, score_stride, 0);
+    if (ws_bytes < L.end) return IDX_ERR_WORKSPACE;
+    ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                R, scores, score_stride, score_stride, static_cast<char*>(workspace), L,
+                static_cast<cudaStream_t>(stream), dev.num_sms};
+    return run_score(a);
+}
+
+idx_status idx_topk(const float* scores, int64_t score_stride, const int32_t* row_lens, int R, int k,
+                    int32_t* indices, void* workspace, size_t ws_bytes, void* stream) {
+    if (!scores || !row_lens || !indices) return IDX_ERR_ARG;
+    if (R < 1 || R > kMaxRows || k < 1 || k > IDX_MAX_K) return IDX_ERR_ARG;
+    if (score_stride < 4 || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
+    uint32_t* status = nullptr;
+    if (workspace) {
+        if (ws_bytes < 256) return IDX_ERR_WORKSPACE;
+        status = static_cast<uint32_t*>(workspace);
+    }
+    DeviceInfo dev;
+    idx_status st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    SelectArgs s{scores, score_stride, row_lens, R, k, indices, status, score_stride,
+                 static_cast<cudaStream_t>(stream)};
+    return to_status(launch_select(s));
+}
+
+idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                          const float* k_scale, int64_t pool_pages, const int32_t* block_table, int max_pages,
+                          const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
+                          int32_t* indices, float* scores, int64_t score_stride, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
+                                     seq_lens, row_req, R, workspace);
+    if (st != IDX_OK) return st;
+    if (!indices || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
+    const int64_t cap = (int64_t)max_pages * kPage;
+    if (max_len > cap) max_len = cap;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    const int with_scores = scores == nullptr;
+    const WsLayout L = ws_layout(R, max_len, with_scores);
+    if (ws_bytes < L.end) return IDX_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    if (with_scores) {
+        scores = reinterpret_cast<float*>(ws + L.scores);
+        score_stride = L.score_stride;
+    } else {
+        if (score_stride < max_len || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
+    st = run_score(a);
+    if (st != IDX_OK) return st;
+    // The plan's clamped row lengths bound each row's selection.
+    const int32_t* row_lens = reinterpret_cast<const Plan*>(ws + L.plan)->row_len;
+    SelectArgs sel{scores, score_stride, row_lens, R, k, indices,
+                   reinterpret_cast<uint32_t*>(ws + L.status), max_len, s};
+    return to_status(launch_select(sel));
+}
+
+idx_status idx_check_status(void* workspace, void* stream) {
+    if (!workspace) return IDX_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    if (word & kStatusTimeout) return IDX_ERR_TIMEOUT;
+    if (word & kStatusBounds) return IDX_ERR_BOUNDS;
+    return IDX_OK;
+}
+
+const char* idx_status_str(int status) {
+    switch (status) {
+        case IDX_OK: return "ok";
+        case IDX_ERR_ARG: return "invalid argument";
+        case IDX_ERR_ALIGN: return "misaligned pointer or stride";
+        case IDX_ERR_WORKSPACE: return "workspace missing or too small";
+        case IDX_ERR_CUDA: return "CUDA error";
+        case IDX_ERR_TIMEOUT: return "device wait timed out";
+        case IDX_ERR_BOUNDS: return "block-table id or row length out of bounds";
+        case IDX_ERR_UNSUPPORTED: return "unsupported device or driver";
+        default: return "unknown status";
+    }
+}
+
+int idx_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+"""The five configurations end to end through idx_score_topk (the launch the
+benchmark times): every score within 1e-4 of the f64 oracle (the largest
+configuration on sampled positions), and every row's list bit-exact against
+the oracle's selection of the GPU's own scores."""
+import numpy as np
+import pytest
+
+import oracle
+from key_scoring_exact_gb300 import workloads as W
+from tests import checks
+from tests.gpu_util import device_inputs, gpu_fused, problem
+
+pytestmark = pytest.mark.gpu
+
+
+def _lists_exact(w, s, got):
+    for r, n in enumerate(w.seq_lens.tolist()):
+        exp = oracle.topk(s[r, :n], w.k)
+        assert np.array_equal(got[r], exp), "row %d list differs" % r
+        assert checks.list_invariants(got[r], s[r, :n], w.k) == []
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_config_full(idx):
+    w = W.make_config(idx)
+    s, got, st = gpu_fused(w)
+    assert st == 0
+    ref = oracle.scores(problem(w))
+    errs = checks.score_errors(s, ref, w.seq_lens.tolist())
+    assert max(errs) <= checks.SCORE_TOL, errs
+    print("config %d: worst relative score error %.3g" % (idx, max(errs)))
+    _lists_exact(w, s, got)
+
+
+def test_config5_sampled():
+    w = W.make_config(5)
+    s, got, st = gpu_fused(w)
+    assert st == 0
+    pb = problem(w)
+    rng = np.random.default_rng(55)
+    worst = 0.0
+    for r, n in enumerate(w.seq_lens.tolist()):
+        pos = np.unique(np.concatenate([[0, 1, 63, 64, 127, 128, n - 2, n - 1],
+                                        rng.integers(0, n, 40),
+                                        np.argsort(-s[r, :n])[:8]])).astype(np.int64)
+        ref = oracle.score_positions(pb, r, pos)
+        # the row's largest reference score, from its top GPU candidates
+        denom = np.max(np.abs(ref))
+        err = np.max(np.abs(s[r, pos] - ref)) / denom
+        worst = max(worst, err)
+    assert worst <= checks.SCORE_TOL, worst
+    print("config 5: worst sampled relative score error %.3g" % worst)
+    _lists_exact(w, s, got)
+
+
+def test_scores_in_workspace():
+    w = W.make_config(1)
+    s1, got1, st1 = gpu_fused(w)
+    s2, got2, st2 = gpu_fused(w, in_workspace=True)
+    assert st1 == 0 and st2 == 0
+    n = w.seq_lens[0].item()
+    assert np.array_equal(s1[:, :n], s2[:, :n]) and np.array_equal(got1, got2)
+
+
+def test_config3_e4m3_query():
+    w = W.make_config(3, q_is_e4m3=True)
+    s, got, st = gpu_fused(w)
+    assert st == 0
+    ref = oracle.scores(problem(w))
+    errs = checks.score_errors(s, ref, w.seq_lens.tolist())
+    assert max(errs) <= checks.SCORE_TOL, errs
+    _lists_exact(w, s, got)
+
+
+def test_fused_replay_determinism():
+    w = W.make_config(2)
+    t = device_inputs(w)
+    s0, g0, _ = gpu_fused(w, t)
+    for _ in range(10):
+        s1, g1, _ = gpu_fused(w, t)
+        assert np.array_equal(s0, s1) and np.array_equal(g0, g1)

@@ -1,0 +1,130 @@
+"""GPU selection (idx_topk) against the oracle's sort-based list, bit-exact.
+
+Score rows cover the page / tile boundaries and the lengths around k from
+tests/golden/ragged_lengths.json, tie-heavy and all-zero rows, rows whose top
+crowds into their last keys, special values, and rows long enough that a
+slice no longer fits in shared memory."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import checks
+from tests.gpu_util import gpu_topk
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "ragged_lengths.json")))
+LENGTHS = sorted(set(GOLDEN["page_boundary"] + GOLDEN["around_k"] + GOLDEN["tile_boundary"]
+                     + [0, 2, 8192, 131072, 131069, 250000]))
+
+
+def _check_rows(scores, lens, k, got):
+    for r, n in enumerate(lens):
+        exp = oracle.topk(scores[r, :n], k)
+        if not np.array_equal(got[r], exp):
+            bad = np.nonzero(got[r] != exp)[0]
+            raise AssertionError("row %d (n=%d): %d entries differ, first at %d: got %d want %d"
+                                 % (r, n, bad.size, bad[0], got[r][bad[0]], exp[bad[0]]))
+
+
+@pytest.mark.parametrize("n", LENGTHS)
+def test_random_lengths(n):
+    rng = np.random.default_rng(n)
+    k = 2048
+    s = rng.standard_normal((1, max(n, 4))).astype(np.float32) * 10
+    got, st = gpu_topk(s, [n], k)
+    assert st == 0
+    _check_rows(s, [n], k, got)
+
+
+def test_mixed_rows_one_launch():
+    rng = np.random.default_rng(1)
+    lens = [0, 1, 500, 2047, 2048, 2049, 3000, 8192, 40000, 131072, 65, 100000]
+    width = max(lens)
+    s = rng.standard_normal((len(lens), width)).astype(np.float32)
+    got, st = gpu_topk(s, lens, 2048)
+    assert st == 0
+    _check_rows(s, lens, 2048, got)
+
+
+@pytest.mark.parametrize("levels", [1, 2, 4, 17])
+def test_tie_heavy(levels):
+    rng = np.random.default_rng(levels)
+    vals = rng.standard_normal(levels).astype(np.float32)
+    n = 50000
+    s = vals[rng.integers(0, levels, n)][None, :]
+    got, st = gpu_topk(s, [n], 2048)
+    assert st == 0
+    _check_rows(s, [n], 2048, got)
+
+
+def test_all_zero_row_is_iota():
+    s = np.zeros((1, 10000), np.float32)
+    got, st = gpu_topk(s, [10000], 2048)
+    assert st == 0
+    assert np.array_equal(got[0], np.arange(2048))
+
+
+def test_recent_crowded():
+    rng = np.random.default_rng(5)
+    n = 131072
+    s = np.abs(rng.standard_normal(n)).astype(np.float32)
+    s[-4096:] *= 8
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
+    assert checks.list_invariants(got[0], s, 2048) == []
+
+
+def test_special_values():
+    rng = np.random.default_rng(9)
+    n = 9000
+    s = rng.standard_normal(n).astype(np.float32)
+    s[::7] = -0.0
+    s[::11] = 0.0
+    s[::13] = np.nan
+    s[5] = np.inf
+    s[6] = -np.inf
+    s[100:3000] = np.float32(2.0)  # a tie block crossing the threshold
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
+
+
+@pytest.mark.parametrize("k", [1, 7, 100, 1000, 2048])
+def test_various_k(k):
+    rng = np.random.default_rng(k)
+    lens = [5, 3000, 70000]
+    s = (rng.integers(-50, 50, (3, 70000)) / 8).astype(np.float32)
+    got, st = gpu_topk(s, lens, k)
+    assert st == 0
+    _check_rows(s, lens, k, got)
+
+
+def test_scores_past_row_length_are_ignored():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((2, 8000)).astype(np.float32)
+    s[0, 5000:] = np.float32(1e30)
+    s[1, 7000:] = np.nan
+    got, st = gpu_topk(s, [5000, 7000], 2048)
+    assert st == 0
+    _check_rows(s, [5000, 7000], 2048, got)
+
+
+def test_row_longer_than_stride_is_reported():
+    s = np.ones((1, 64), np.float32)
+    got, st = gpu_topk(s, [1000], 8)
+    assert st == -6  # IDX_ERR_BOUNDS: the row is clamped to the stride
+    assert np.array_equal(got[0], np.arange(8))
+
+
+def test_deterministic_replays():
+    rng = np.random.default_rng(11)
+    s = (rng.integers(0, 5, (4, 60000))).astype(np.float32)
+    a, _ = gpu_topk(s, [60000, 59999, 30000, 2049], 2048)
+    for _ in range(5):
+        b, _ = gpu_topk(s, [60000, 59999, 30000, 2049], 2048)
+        assert np.array_equal(a, b)
