@@ -1,0 +1,511 @@
+#!/usr/bin/env python3
+"""Benchmark of the index chain: paged key scoring + exact top-2048.
+
+One step = one idx_score_topk launch sequence (prep, scoring, selection) over
+one batch of synthetic inputs that are already resident in HBM.  The default
+workload is 1 request with 4 verify rows at 131,069..131,072 keys (E4M3 keys
+with per-key scales whose last 4,096 keys are 8x, bf16 query, 64 heads x 128,
+k = 2048).  Successive steps cycle through 16 copies of the key cache
+(277 MB > 2 x L2), so keys stream from HBM.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs, bracketed by CUDA events on the launching stream (and a barrier +
+max over ranks under torchrun).  A second, instrumented replay of the same
+steps records events between the scoring and the selection kernels for the
+per-kernel roofline.  nvidia-smi samples the clocks meanwhile.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
+plain f64 scoring and sort-based selection) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "µs per indexer launch (score + exact top-2048) at 4 rows, 8K/128K keys; keys/s"
+UNIT = "us"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio
+L2_BYTES = 129 * 1024 * 1024
+COPIES = 16
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=3, help="workload configuration 1..5")
+    ap.add_argument("--copies", type=int, default=COPIES)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-8k", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.result = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+        self.path = os.path.join("/tmp", "idx_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        self.result = self._stop()
+        return self.result
+
+    def _stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             parts[5], parts[6], parts[7], parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3:]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+# ---------------------------------------------------------------------- peaks
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def ncu_traffic(kernel: str, source: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    summary, or None when the kernel's source has changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "key_scoring_exact_gb300", "csrc", source)
+    if not os.path.exists(p) or not os.path.exists(src):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ the GPU bench
+
+class Step:
+    """Device buffers for one configuration and its rotation copies."""
+
+    def __init__(self, w, copies, dev):
+        from key_scoring_exact_gb300 import binding, workloads as W
+        self.binding = binding
+        self.w = w
+        big, tables = W.with_rotation(w, copies)
+        self.copies = copies
+        self.q = w.q.to(dev)
+        self.head_w = w.head_w.to(dev)
+        self.k_cache = big.k_cache.to(dev)
+        self.k_scale = big.k_scale.to(dev)
+        self.tables = [tables[c].contiguous().to(dev) for c in range(copies)]
+        self.seq_lens = w.seq_lens.to(dev)
+        self.row_req = w.row_req.to(dev)
+        self.R, self.k, self.max_len = w.R, w.k, w.max_len
+        self.stride = (self.max_len + 3) // 4 * 4
+        self.scores = torch.zeros(self.R, self.stride, dtype=torch.float32, device=dev)
+        self.idx = torch.zeros(self.R, self.k, dtype=torch.int32, device=dev)
+        self.ws = binding.new_workspace(self.R, self.max_len, self.k, device=dev)
+
+    def fused(self, c, stream=None):
+        b = self.binding
+        b.score_topk(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
+                     self.seq_lens, self.row_req, self.max_len, self.k, self.idx, self.ws,
+                     scores=self.scores, stream=stream)
+
+    def score_only(self, c, stream=None):
+        self.binding.score(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
+                           self.seq_lens, self.row_req, self.scores, self.ws, stream=stream)
+
+    def select_only(self, stream=None):
+        self.binding.topk(self.scores, self.seq_lens, self.k, self.idx, self.ws, stream=stream)
+
+    def key_bytes(self):
+        return self.w.unique_key_bytes()
+
+    def alg_bytes_score(self):
+        """HBM bytes the scoring must move: every key + scale once, the query,
+        head weights and block-table entries in, one f32 score per (row, key) out."""
+        w = self.w
+        pages = sum((n + 63) // 64 for n in w.req_keys)
+        return (self.key_bytes() + w.R * 64 * 128 * (1 if w.q_is_e4m3 else 2) + w.R * 64 * 4
+                + pages * 4 + 4 * w.row_keys())
+
+    def alg_bytes_select(self):
+        """HBM bytes of the selection: every score read once, k indices written."""
+        return 4 * self.w.row_keys() + 4 * self.R * self.k
+
+    def alg_flops(self):
+        """MMA flops of the algorithm: 2 * 64 heads * 128 dims per (row, key)."""
+        return 2 * 64 * 128 * self.w.row_keys()
+
+
+def capture(stream, fn, n):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def time_graph_steps(st: Step, steps: int, stream, dist, sampler=None):
+    """Exactly `steps` fused steps replayed from graphs; returns seconds per step."""
+    G = min(steps, 256)
+    full, rem = divmod(steps, G)
+    g_full = capture(stream, lambda i: st.fused(i, stream), G)
+    g_rem = capture(stream, lambda i: st.fused(i, stream), rem) if rem else None
+    g_full.replay()  # upload + warm
+    if g_rem is not None:
+        g_rem.replay()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
+    e0.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.stop()
+    barrier(dist)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
+def _graph_event():
+    """A timing event that records as a node inside a captured graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def per_kernel_times(st: Step, n: int, stream):
+    """Events around the scoring (prep + score kernels) and the selection
+    kernel of n steps, replayed from one graph; returns mean seconds each."""
+    if _graph_event() is None:
+        return per_kernel_times_eager(st, n, stream)
+    ev = [[_graph_event() for _ in range(3)] for _ in range(n)]
+
+    def body(i):
+        ev[i][0].record(stream)
+        st.score_only(i, stream)
+        ev[i][1].record(stream)
+        st.select_only(stream)
+        ev[i][2].record(stream)
+
+    g = capture(stream, body, n)
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = [e[0].elapsed_time(e[1]) / 1e3 for e in ev]
+    tk = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
+    return float(np.mean(ts)), float(np.mean(tk))
+
+
+def per_kernel_times_eager(st: Step, n: int, stream):
+    """Fallback without graph event nodes: eager steps, events on the stream."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        st.score_only(i, stream)
+        ev[i][1].record(stream)
+        st.select_only(stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    ts = [e[0].elapsed_time(e[1]) / 1e3 for e in ev]
+    tk = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
+    return float(np.median(ts)), float(np.median(tk))
+
+
+def copies_for(w, minimum: int) -> int:
+    """Key-cache copies whose total exceeds 2.1 x L2."""
+    need = int(np.ceil(2.1 * L2_BYTES / max(1, w.unique_key_bytes())))
+    return max(minimum, need)
+
+
+def e2e_time(st: Step, steps: int, stream):
+    """Through the public API with host buffers: per step, pinned H2D of the
+    step's inputs (query, head weights, block table, row lengths, row map),
+    idx_score_topk, D2H of the indices.  The key cache is device-resident
+    state (the serving KV cache), not a per-step input."""
+    w = st.w
+    host_in = {"q": w.q.pin_memory(), "head_w": w.head_w.pin_memory(),
+               "tables": [t.cpu().pin_memory() for t in st.tables],
+               "seq_lens": w.seq_lens.pin_memory(), "row_req": w.row_req.pin_memory()}
+    out_host = torch.empty(st.R, st.k, dtype=torch.int32).pin_memory()
+    dq, dw = torch.empty_like(st.q), torch.empty_like(st.head_w)
+    dl, dr = torch.empty_like(st.seq_lens), torch.empty_like(st.row_req)
+    dt = torch.empty_like(st.tables[0])
+    h2d = (host_in["q"].numel() * host_in["q"].element_size() + host_in["head_w"].numel() * 4
+           + host_in["tables"][0].numel() * 4 + 2 * st.R * 4)
+    d2h = st.R * st.k * 4
+    b = st.binding
+
+    def one(i):
+        dq.copy_(host_in["q"], non_blocking=True)
+        dw.copy_(host_in["head_w"], non_blocking=True)
+        dt.copy_(host_in["tables"][i % st.copies], non_blocking=True)
+        dl.copy_(host_in["seq_lens"], non_blocking=True)
+        dr.copy_(host_in["row_req"], non_blocking=True)
+        b.score_topk(dq, dw, st.k_cache, st.k_scale, dt, dl, dr, st.max_len, st.k, st.idx, st.ws,
+                     scores=st.scores, stream=stream)
+        out_host.copy_(st.idx, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def _oracle_run(w, keys_per_row: int):
+    """Oracle scores of every row over its first keys_per_row keys, then the
+    sort-based top-k of those scores.  Returns (seconds, row-keys done)."""
+    import oracle
+    lens = w.seq_lens.numpy()
+    sample = np.minimum(lens, max(1, int(keys_per_row))).astype(np.int32)
+    pb = oracle.Problem(w.q_bits().numpy(), w.q_is_e4m3, w.head_w.numpy(), w.k_cache.numpy(),
+                        w.k_scale.numpy(), w.block_table.numpy(), sample, w.row_req.numpy())
+    t0 = time.perf_counter()
+    s = oracle.scores(pb)
+    for r in range(w.R):
+        oracle.topk(s[r, :sample[r]].astype(np.float32), w.k)
+    return time.perf_counter() - t0, int(sample.sum())
+
+
+def oracle_launch_time(w, budget_s: float):
+    """The oracle as it stands, timed on a bounded sample sized to take about
+    budget_s seconds, scaled to one whole launch (per row-key).  Single-threaded."""
+    lens = w.seq_lens.numpy()
+    t, done = _oracle_run(w, 256)                       # calibration
+    per_rowkey = t / done
+    keys = int(min(lens.max(), max(256, budget_s / per_rowkey / w.R)))
+    t, done = _oracle_run(w, keys)
+    total = float(lens.sum())
+    desc = ("all %d rows over their first %d keys: %d of %d row-keys (%.3g of the launch), "
+            "time scaled by row-keys" % (w.R, keys, done, int(total), done / total))
+    return t * total / done, desc
+
+
+def reference_main(args, w):
+    dist, rank, world, _ = dist_setup(args)
+    if rank != 0:
+        return
+    # the whole run (warm-up + steps) stays within about two minutes
+    per_step = max(0.02, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        t, desc = oracle_launch_time(w, per_step)
+        if i >= args.warmup:
+            times.append(t)
+    us = float(np.mean(times)) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_desc(w, args),
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_desc(w, args):
+    return {"workload": "config %d: %s" % (args.config, w.recipe), "rows": w.R,
+            "requests": len(w.req_keys), "keys_per_row": [int(x) for x in w.seq_lens.tolist()][:8],
+            "heads": 64, "dim": 128, "page": 64, "k": w.k, "query": "bf16" if not w.q_is_e4m3 else "e4m3",
+            "l2": "inputs rotate over %d key-cache copies (%.0f MB > 2x L2)" % (
+                args.copies, args.copies * w.unique_key_bytes() / 1e6),
+            "parallelism": "replicas" if args.gpus > 1 else "1 GPU"}
+
+
+def main():
+    args = parse()
+    from key_scoring_exact_gb300 import workloads as W
+    w = W.make_config(args.config)
+    if args.impl == "reference":
+        reference_main(args, w)
+        return
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        sys.exit(1)
+    dist, rank, world, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from key_scoring_exact_gb300 import binding
+    binding.load(build_if_missing=True)
+    stream = torch.cuda.Stream(device=dev)
+    args.copies = copies_for(w, args.copies)
+    st = Step(w, args.copies, dev)
+
+    sampler = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            st.fused(i, stream)
+        torch.cuda.synchronize()
+        if binding.check_status(st.ws, stream) != 0:
+            raise RuntimeError("device status after warm-up")
+        sec = time_graph_steps(st, args.steps, stream, dist, sampler)
+    clocks = sampler.result
+    sec = max_over_ranks(dist, sec)
+    with torch.cuda.stream(stream):
+        t_score, t_select = per_kernel_times(st, min(args.steps, 64), stream)
+        status = binding.check_status(st.ws, stream)
+    if status != 0:
+        raise RuntimeError("device status %d after the timed steps" % status)
+
+    hbm, bf16, bf16_sus, src = peaks()
+    score_bytes = st.alg_bytes_score()
+    select_bytes = st.alg_bytes_select()
+    roof_score = {"kernel": "scoring (k_prep + k_score)", "bound": "hbm",
+                  "achieved": score_bytes / t_score / 1e9, "peak": hbm, "unit": "GB/s",
+                  "frac": score_bytes / t_score / 1e9 / hbm, "traffic": ncu_traffic("k_score", "score.cu"),
+                  "alg_bytes": score_bytes, "us": t_score * 1e6, "peak_source": src}
+    roof_select = {"kernel": "k_select", "bound": "hbm",
+                   "achieved": select_bytes / t_select / 1e9, "peak": hbm, "unit": "GB/s",
+                   "frac": select_bytes / t_select / 1e9 / hbm, "traffic": ncu_traffic("k_select", "select.cu"),
+                   "alg_bytes": select_bytes, "us": t_select * 1e6, "peak_source": src}
+    dominant, other = (roof_score, roof_select) if t_score >= t_select else (roof_select, roof_score)
+    fused_bytes = st.key_bytes() + 4 * st.R * st.k
+    line = {
+        "metric": METRIC, "value": sec * 1e6, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 MMA, f32 accumulate, u32 radix", "data": "synthetic",
+        "config": config_desc(w, args),
+        "keys_per_s": world * w.row_keys() / sec,
+        "unique_keys_per_s": world * sum(w.req_keys) / sec,
+        "roofline": dominant,
+        "roofline_other": other,
+        "roofline_fused": {"alg_bytes": fused_bytes, "roof_us": fused_bytes / hbm / 1e3,
+                           "frac": fused_bytes / hbm / 1e3 / (sec * 1e6)},
+        "mma": {"alg_flops": st.alg_flops(), "executed_flops": st.alg_flops() * (1 if w.q_is_e4m3 else 2),
+                "fp8_peak_tflops": bf16 * FP8_OVER_BF16,
+                "alg_tflops_in_scoring": st.alg_flops() / t_score / 1e12},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_8k:
+        w8 = W.make_config(2)
+        st8 = Step(w8, copies_for(w8, args.copies), dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                st8.fused(i, stream)
+            sec8 = time_graph_steps(st8, min(args.steps, 1024), stream, None)
+        line["also_8k"] = {"workload": "config 2: " + w8.recipe, "us": sec8 * 1e6,
+                           "keys_per_s": w8.row_keys() / sec8}
+        del st8
+    if not args.no_e2e:
+        e2e_sec, h2d, d2h = e2e_time(st, min(args.steps, 200), stream)
+        line["e2e"] = {"value": e2e_sec * 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        t, desc = oracle_launch_time(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": t * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -43,6 +43,7 @@ extern "C" {
 #define IDX_MAX_K 2048    /* largest k of the top-k */
 #define IDX_MAX_ROWS 1024 /* most query rows in one call */
 #define IDX_GROUP_ROWS 4  /* rows of one request scored in one pass */
+#define IDX_MAX_TOPK_LEN 524288 /* longest row the top-k selection takes */
 
 typedef enum {
     IDX_OK = 0,
@@ -114,7 +115,9 @@ idx_status idx_score(int qtype, const void *q, const float *head_w,
  * -0 == +0; a NaN ranks below every number (finite inputs are expected).
  *
  *  scores       [R][score_stride] f32, 16-byte aligned, score_stride % 4 == 0
- *  row_lens     [R] int32, each in [0, score_stride]
+ *  row_lens     [R] int32, each in [0, min(score_stride, IDX_MAX_TOPK_LEN)];
+ *               a longer row is cut to that length and reported as
+ *               IDX_ERR_BOUNDS by idx_check_status
  *  k            1 .. IDX_MAX_K
  *  indices      [R][k] int32 out
  *  workspace    status word holder (>= idx_workspace_bytes(R, score_stride, k, 0)
@@ -130,7 +133,9 @@ idx_status idx_topk(const float *scores, int64_t score_stride, const int32_t *ro
  * idx_score_topk -- idx_score then idx_topk on the same stream, with no host
  * round trip in between.  scores may be NULL: the scores then live in the
  * workspace (size it with with_scores = 1) and score_stride is ignored.
- * max_len bounds the longest row (used for the launch shape and workspace).
+ * max_len bounds the longest row (used for the launch shape and workspace);
+ * it must not exceed IDX_MAX_TOPK_LEN (IDX_ERR_ARG), and rows longer than
+ * max_len are cut to it (IDX_ERR_BOUNDS).
  */
 idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,

@@ -161,7 +161,8 @@ idx_status idx_topk(const float* scores, int64_t score_stride, const int32_t* ro
     DeviceInfo dev;
     idx_status st = device_info(&dev);
     if (st != IDX_OK) return st;
-    SelectArgs s{scores, score_stride, row_lens, R, k, indices, status, score_stride,
+    const int64_t bound = score_stride < kSelectMaxLen ? score_stride : kSelectMaxLen;
+    SelectArgs s{scores, score_stride, row_lens, R, k, indices, status, bound,
                  static_cast<cudaStream_t>(stream)};
     return to_status(launch_select(s));
 }
@@ -177,6 +178,7 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
     if (!indices || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
     const int64_t cap = (int64_t)max_pages * kPage;
     if (max_len > cap) max_len = cap;
+    if (max_len > kSelectMaxLen) return IDX_ERR_ARG;
     DeviceInfo dev;
     st = device_info(&dev);
     if (st != IDX_OK) return st;

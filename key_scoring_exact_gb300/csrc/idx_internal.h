@@ -111,5 +111,8 @@ struct SelectArgs {
 };
 
 cudaError_t launch_select(const SelectArgs& a);
+// Longest row the selection handles with clusters of `cluster` CTAs.
+int64_t select_max_len(int cluster);
+constexpr int64_t kSelectMaxLen = 16 * 512 * 4 * 16;  // 524,288 keys (16-CTA clusters)
 
 }  // namespace idx

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(int qtype, const void* q,
                                                        const int32_t* seq_lens, const int32_t* row_req,
                                                        int R, int max_pages, int64_t len_bound, uint8_t* q8,
                                                        float* wq, Plan* plan, uint32_t* status, int n_qblocks) {
+    pdl_launch_dependents();  // the scoring kernel may start its set-up now
     if ((int)blockIdx.x == n_qblocks) {
         build_plan(seq_lens, row_req, R, max_pages, len_bound, plan, status);
         return;
@@ -184,6 +185,18 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(int qtype, const void* q,
 }  // namespace
 
 cudaError_t launch_prep(const ScoreArgs& a) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        // Same shared-memory carve-out as the scoring kernel that follows, so
+        // an SM need not drain and reconfigure between the two launches.
+        err = cudaFuncSetAttribute(k_prep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+        configured_device = dev;
+    }
     const int n_qblocks = (a.R * kHeads + kPairsPerBlock - 1) / kPairsPerBlock;
     k_prep<<<n_qblocks + 1, kPrepThreads, 0, a.stream>>>(
         a.qtype, a.q, a.head_w, a.seq_lens, a.row_req, a.R, a.max_pages, a.len_bound,
