@@ -145,6 +145,38 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           float *scores, int64_t score_stride,
                           void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * idx_score_noalloc -- idx_score for callers that cannot allocate device
+ * memory, with no workspace argument.  The paper has no counterpart to this
+ * entry point; it exists for callers such as a serving loop replaying a
+ * captured CUDA graph, an allocator-less embedding, or code inside a memory
+ * pool that forbids new allocations, which cannot obtain (or size) a
+ * workspace buffer.
+ *
+ * Arguments, layouts and results are those of idx_score minus the workspace.
+ * Instead of a workspace, the call uses one fixed scratch array in device
+ * memory that the library declares statically (about 1.1 MB; every device
+ * that loads the library holds it until the process exits).  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *  - R must be in [1, IDX_NOALLOC_MAX_ROWS]; larger R returns IDX_ERR_ARG.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array.  Calls whose work overlaps on the GPU
+ *    (different streams without ordering, or several host threads) race and
+ *    may corrupt each other's results; serialise them.  Every call rewrites
+ *    all the scratch it reads, so nothing needs clearing between calls.
+ *  - Device-detected problems (a block-table id outside the pool, a row
+ *    longer than its block table or the score buffer) are handled as in
+ *    idx_score but not reported: there is no status word to read them from.
+ */
+#define IDX_NOALLOC_MAX_ROWS 64
+idx_status idx_score_noalloc(int qtype, const void *q, const float *head_w,
+                             const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                             const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, const int32_t *row_req, int R,
+                             float *scores, int64_t score_stride, void *stream);
+
 /* Wait for `stream`, read and clear the workspace status word, and return the
  * first device error recorded since the last call (IDX_OK if none). */
 idx_status idx_check_status(void *workspace, void *stream);

@@ -21,7 +21,7 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
           -4: "IDX_ERR_CUDA", -5: "IDX_ERR_TIMEOUT", -6: "IDX_ERR_BOUNDS", -7: "IDX_ERR_UNSUPPORTED"}
 
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
-           "idx_check_status", "idx_status_str", "idx_version")
+           "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc")
 
 _lib = None
 
@@ -65,6 +65,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_status_str.argtypes = [i32]
     lib.idx_version.restype = i32
     lib.idx_version.argtypes = []
+    lib.idx_score_noalloc.restype = i32
+    lib.idx_score_noalloc.argtypes = score_common + [p, i64, p]
     _lib = lib
     return lib
 
@@ -140,6 +142,18 @@ def score(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, w
     st = load().idx_score(*args, _dev(scores, "scores", torch.float32), int(scores.shape[1]),
                           _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "idx_score")
+
+
+def score_noalloc(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, stream=None):
+    """idx_score_noalloc: idx_score without a workspace, for callers that
+    cannot allocate; it uses the library's one static scratch array, so calls
+    must not overlap on the GPU.  At most 64 rows."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
+    if scores.dim() != 2 or scores.shape[0] != q.shape[0]:
+        raise ValueError("scores must be [R, stride]")
+    st = load().idx_score_noalloc(*args, _dev(scores, "scores", torch.float32), int(scores.shape[1]),
+                                  _stream(stream))
+    _check(st, "idx_score_noalloc")
 
 
 def topk(scores, row_lens, k, indices, workspace=None, stream=None):

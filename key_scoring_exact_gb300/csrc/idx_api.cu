@@ -109,6 +109,42 @@ idx_status run_score(const ScoreArgs& a) {
     return to_status(launch_score(a, keys_map, q_map));
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for idx_score_noalloc: a fixed device array instead of a caller
+// workspace.  Its size covers the workspace layout of IDX_NOALLOC_MAX_ROWS
+// rows (status word, plan, scaled head weights, split query); every device
+// that loads this library keeps it for the life of the process.
+constexpr size_t kNoallocScratchBytes =
+    1024 + ((sizeof(Plan) + 1023) / 1024) * 1024 +
+    ((sizeof(float) * IDX_NOALLOC_MAX_ROWS * kHeads + 1023) / 1024) * 1024 +
+    ((size_t)2 * IDX_NOALLOC_MAX_ROWS * kHeads * kDim + 1023) / 1024 * 1024;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// The array's device address, looked up once per device with that device
+// current (in host code the array's name is only a stand-in for it).
+idx_status noalloc_scratch(char** out) {
+    static std::mutex mu;
+    static char* addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64) return IDX_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return IDX_ERR_CUDA;
+        }
+        addr[dev] = static_cast<char*>(p);
+    }
+    *out = addr[dev];
+    return IDX_OK;
+}
+
 }  // namespace
 }  // namespace idx
 
@@ -231,6 +267,33 @@ const char* idx_status_str(int status) {
         case IDX_ERR_UNSUPPORTED: return "unsupported device or driver";
         default: return "unknown status";
     }
+}
+
+idx_status idx_score_noalloc(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                             const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                             int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                             float* scores, int64_t score_stride, void* stream) {
+    if (R < 1 || R > IDX_NOALLOC_MAX_ROWS) return IDX_ERR_ARG;  // the static scratch holds this many rows
+    // The checks of idx_score, minus the workspace (the scratch array is 256-byte aligned).
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (!q || !head_w || !k_cache || !k_scale || !block_table || !seq_lens || !row_req) return IDX_ERR_ARG;
+    if (pool_pages < 1 || pool_pages > (int64_t(1) << 25)) return IDX_ERR_ARG;
+    if (max_pages < 1 || (int64_t)max_pages * kPage > INT32_MAX) return IDX_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(k_scale, 16)) return IDX_ERR_ALIGN;
+    if (!scores) return IDX_ERR_ARG;
+    if (score_stride < 4 || score_stride % 4 != 0) return IDX_ERR_ALIGN;
+    if (!aligned(scores, 16)) return IDX_ERR_ALIGN;
+    DeviceInfo dev;
+    idx_status st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    char* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != IDX_OK) return st;
+    const WsLayout L = ws_layout(R, score_stride, 0);
+    if (L.end > kNoallocScratchBytes) return IDX_ERR_WORKSPACE;
+    ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                R, scores, score_stride, score_stride, scratch, L, static_cast<cudaStream_t>(stream), dev.num_sms};
+    return run_score(a);
 }
 
 int idx_version(void) { return 100; }
