@@ -1,18 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark of the index chain: paged key scoring + exact top-2048.
 
-One step = one idx_score_topk launch sequence (prep, scoring, selection) over
+One step = one idx_score_topk launch sequence (scoring, selection) over
 one batch of synthetic inputs that are already resident in HBM.  The default
 workload is 1 request with 4 verify rows at 131,069..131,072 keys (E4M3 keys
 with per-key scales whose last 4,096 keys are 8x, bf16 query, 64 heads x 128,
-k = 2048).  Successive steps cycle through 16 copies of the key cache
-(277 MB > 2 x L2), so keys stream from HBM.
+k = 2048).  Successive steps cycle through enough copies of the key cache
+to exceed 2.1 x L2 (17 copies, 294 MB), so keys stream from HBM.
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs, bracketed by CUDA events on the launching stream (and a barrier +
-max over ranks under torchrun).  A second, instrumented replay of the same
-steps records events between the scoring and the selection kernels for the
-per-kernel roofline.  nvidia-smi samples the clocks meanwhile.
+max over ranks under torchrun).  For the per-kernel roofline, each of the two
+kernels is then replayed alone from a graph of its own launches, bracketed by
+CUDA events.  nvidia-smi samples the clocks during the timed steps.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
 plain f64 scoring and sort-based selection) on a bounded sample.
@@ -263,51 +263,26 @@ def time_graph_steps(st: Step, steps: int, stream, dist, sampler=None):
     return e0.elapsed_time(e1) / 1e3 / steps
 
 
-def _graph_event():
-    """A timing event that records as a node inside a captured graph."""
-    try:
-        return torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        return None
-
-
 def per_kernel_times(st: Step, n: int, stream):
-    """Events around the scoring (prep + score kernels) and the selection
-    kernel of n steps, replayed from one graph; returns mean seconds each."""
-    if _graph_event() is None:
-        return per_kernel_times_eager(st, n, stream)
-    ev = [[_graph_event() for _ in range(3)] for _ in range(n)]
-
-    def body(i):
-        ev[i][0].record(stream)
-        st.score_only(i, stream)
-        ev[i][1].record(stream)
-        st.select_only(stream)
-        ev[i][2].record(stream)
-
-    g = capture(stream, body, n)
-    g.replay()
-    torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    ts = [e[0].elapsed_time(e[1]) / 1e3 for e in ev]
-    tk = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
-    return float(np.mean(ts)), float(np.mean(tk))
-
-
-def per_kernel_times_eager(st: Step, n: int, stream):
-    """Fallback without graph event nodes: eager steps, events on the stream."""
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-    for i in range(n):
-        ev[i][0].record(stream)
-        st.score_only(i, stream)
-        ev[i][1].record(stream)
-        st.select_only(stream)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    ts = [e[0].elapsed_time(e[1]) / 1e3 for e in ev]
-    tk = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
-    return float(np.median(ts)), float(np.median(tk))
+    """Average launch duration of each kernel: n scoring launches (rotating
+    key-cache copies) replayed from one graph, then n selection launches from
+    another, each bracketed by CUDA events on the launching stream.  Timing
+    each kernel in a graph of its own keeps the launch pipelined, as it is in
+    the fused steps; events placed between the two kernels of every step
+    would add the launch latency to both.  Returns mean seconds of each."""
+    out = []
+    for body in (lambda i: st.score_only(i, stream), lambda i: st.select_only(stream)):
+        g = capture(stream, body, n)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / 1e3 / n)
+        del g
+    return out[0], out[1]
 
 
 def copies_for(w, minimum: int) -> int:
@@ -411,7 +386,7 @@ def reference_main(args, w):
 
 
 def config_desc(w, args):
-    return {"workload": "config %d: %s" % (args.config, w.recipe), "rows": w.R,
+    return {"workload": w.recipe, "rows": w.R,
             "requests": len(w.req_keys), "keys_per_row": [int(x) for x in w.seq_lens.tolist()][:8],
             "heads": 64, "dim": 128, "page": 64, "k": w.k, "query": "bf16" if not w.q_is_e4m3 else "e4m3",
             "l2": "inputs rotate over %d key-cache copies (%.0f MB > 2x L2)" % (
@@ -449,7 +424,7 @@ def main():
     clocks = sampler.result
     sec = max_over_ranks(dist, sec)
     with torch.cuda.stream(stream):
-        t_score, t_select = per_kernel_times(st, min(args.steps, 64), stream)
+        t_score, t_select = per_kernel_times(st, min(args.steps, 256), stream)
         status = binding.check_status(st.ws, stream)
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
@@ -457,7 +432,7 @@ def main():
     hbm, bf16, bf16_sus, src = peaks()
     score_bytes = st.alg_bytes_score()
     select_bytes = st.alg_bytes_select()
-    roof_score = {"kernel": "scoring (k_prep + k_score)", "bound": "hbm",
+    roof_score = {"kernel": "k_score", "bound": "hbm",
                   "achieved": score_bytes / t_score / 1e9, "peak": hbm, "unit": "GB/s",
                   "frac": score_bytes / t_score / 1e9 / hbm, "traffic": ncu_traffic("k_score", "score.cu"),
                   "alg_bytes": score_bytes, "us": t_score * 1e6, "peak_source": src}
@@ -481,7 +456,7 @@ def main():
         "mma": {"alg_flops": st.alg_flops(), "executed_flops": st.alg_flops() * (1 if w.q_is_e4m3 else 2),
                 "fp8_peak_tflops": bf16 * FP8_OVER_BF16,
                 "alg_tflops_in_scoring": st.alg_flops() / t_score / 1e12},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
     if not args.no_8k:
@@ -491,7 +466,7 @@ def main():
             for i in range(3):
                 st8.fused(i, stream)
             sec8 = time_graph_steps(st8, min(args.steps, 1024), stream, None)
-        line["also_8k"] = {"workload": "config 2: " + w8.recipe, "us": sec8 * 1e6,
+        line["also_8k"] = {"workload": w8.recipe, "us": sec8 * 1e6,
                            "keys_per_s": w8.row_keys() / sec8}
         del st8
     if not args.no_e2e:

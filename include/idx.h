@@ -155,22 +155,22 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
  *
  * Arguments, layouts and results are those of idx_score minus the workspace.
  * Instead of a workspace, the call uses one fixed scratch array in device
- * memory that the library declares statically (about 1.1 MB; every device
- * that loads the library holds it until the process exits).  Nothing is
- * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ * memory that the library declares statically (1 KB holding the call's status
+ * word; every device that loads the library holds it until the process
+ * exits).  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
  *
  *  - R must be in [1, IDX_NOALLOC_MAX_ROWS]; larger R returns IDX_ERR_ARG.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - All calls share the one array.  Calls whose work overlaps on the GPU
- *    (different streams without ordering, or several host threads) race and
- *    may corrupt each other's results; serialise them.  Every call rewrites
- *    all the scratch it reads, so nothing needs clearing between calls.
+ *    (different streams without ordering, or several host threads) share its
+ *    status word; nothing else is shared, and nothing needs clearing.
  *  - Device-detected problems (a block-table id outside the pool, a row
  *    longer than its block table or the score buffer) are handled as in
  *    idx_score but not reported: there is no status word to read them from.
  */
-#define IDX_NOALLOC_MAX_ROWS 64
+#define IDX_NOALLOC_MAX_ROWS IDX_MAX_ROWS
 idx_status idx_score_noalloc(int qtype, const void *q, const float *head_w,
                              const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
                              const int32_t *block_table, int max_pages,

@@ -146,8 +146,8 @@ def score(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, w
 
 def score_noalloc(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, stream=None):
     """idx_score_noalloc: idx_score without a workspace, for callers that
-    cannot allocate; it uses the library's one static scratch array, so calls
-    must not overlap on the GPU.  At most 64 rows."""
+    cannot allocate; it uses the library's one static scratch array (its
+    status word), and device-side bounds problems are not reported."""
     args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
     if scores.dim() != 2 or scores.shape[0] != q.shape[0]:
         raise ValueError("scores must be [R, stride]")

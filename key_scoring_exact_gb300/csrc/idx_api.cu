@@ -99,25 +99,18 @@ idx_status to_status(cudaError_t e) {
 }
 
 idx_status run_score(const ScoreArgs& a) {
-    CUtensorMap keys_map, q_map;
+    CUtensorMap keys_map;
     idx_status st = make_rows_map(&keys_map, a.k_cache, (uint64_t)a.pool_pages * kPage);
     if (st != IDX_OK) return st;
-    st = make_rows_map(&q_map, a.ws + a.L.q8, (uint64_t)2 * a.R * kHeads);
-    if (st != IDX_OK) return st;
-    st = to_status(launch_prep(a));
-    if (st != IDX_OK) return st;
-    return to_status(launch_score(a, keys_map, q_map));
+    return to_status(launch_score(a, keys_map));
 }
 
 // ---------------------------------------------------------------------------
 // Scratch for idx_score_noalloc: a fixed device array instead of a caller
-// workspace.  Its size covers the workspace layout of IDX_NOALLOC_MAX_ROWS
-// rows (status word, plan, scaled head weights, split query); every device
-// that loads this library keeps it for the life of the process.
-constexpr size_t kNoallocScratchBytes =
-    1024 + ((sizeof(Plan) + 1023) / 1024) * 1024 +
-    ((sizeof(float) * IDX_NOALLOC_MAX_ROWS * kHeads + 1023) / 1024) * 1024 +
-    ((size_t)2 * IDX_NOALLOC_MAX_ROWS * kHeads * kDim + 1023) / 1024 * 1024;
+// workspace.  It holds the part of the workspace layout the scoring kernel
+// uses (its status word); every device that loads this library keeps it for
+// the life of the process.
+constexpr size_t kNoallocScratchBytes = 1024;  // the status word's block of the workspace layout
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -198,7 +191,7 @@ idx_status idx_topk(const float* scores, int64_t score_stride, const int32_t* ro
     idx_status st = device_info(&dev);
     if (st != IDX_OK) return st;
     const int64_t bound = score_stride < kSelectMaxLen ? score_stride : kSelectMaxLen;
-    SelectArgs s{scores, score_stride, row_lens, R, k, indices, status, bound,
+    SelectArgs s{scores, score_stride, row_lens, R, k, indices, status, bound, score_stride,
                  static_cast<cudaStream_t>(stream)};
     return to_status(launch_select(s));
 }
@@ -233,10 +226,9 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
                 R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
     st = run_score(a);
     if (st != IDX_OK) return st;
-    // The plan's clamped row lengths bound each row's selection.
-    const int32_t* row_lens = reinterpret_cast<const Plan*>(ws + L.plan)->row_len;
-    SelectArgs sel{scores, score_stride, row_lens, R, k, indices,
-                   reinterpret_cast<uint32_t*>(ws + L.status), max_len, s};
+    // Each row's selection covers the keys its scores were written for.
+    SelectArgs sel{scores, score_stride, seq_lens, R, k, indices,
+                   reinterpret_cast<uint32_t*>(ws + L.status), max_len, max_len, s};
     return to_status(launch_select(sel));
 }
 

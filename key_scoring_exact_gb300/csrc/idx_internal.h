@@ -24,28 +24,10 @@ constexpr int kSelectThreads = 256;
 constexpr uint32_t kStatusBounds = 1u;   // block-table id outside the pool / row too long
 constexpr uint32_t kStatusTimeout = 2u;  // a bounded wait gave up
 
-// Scoring plan written by the prep kernel: rows grouped by request (at most
-// kGroupRows consecutive rows of one request per group) and the groups' tiles
-// numbered in one sequence of work items.
-struct Plan {
-    int n_groups;
-    int n_items;
-    int pad[62];
-    int g_req[kMaxRows];
-    int g_r0[kMaxRows];
-    int g_nr[kMaxRows];
-    int g_len[kMaxRows];            // longest row of the group (clamped)
-    int g_item[kMaxRows + 1];       // first work item of each group
-    int row_len[kMaxRows];          // seq_lens clamped to the block table
-};
-
-// Workspace layout (every block 1024-byte aligned).
+// Workspace layout: the status word, then (optionally) an f32 score matrix.
 struct WsLayout {
     size_t status;   // uint32 status word
-    size_t plan;     // Plan
-    size_t wq;       // f32 [R][64]: head weights with the query's power-of-two scale folded in
-    size_t q8;       // u8 [2][R][64][128]: the query as E4M3 hi / lo parts
-    size_t scores;   // f32 [R][stride] (optional)
+    size_t scores;   // f32 [R][score_stride] (optional)
     size_t end;
     int64_t score_stride;
 };
@@ -54,20 +36,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline WsLayout ws_layout(int R, int64_t max_len, int with_scores) {
     WsLayout L{};
-    size_t off = 0;
-    L.status = off;
-    off = align_up(off + 256, 1024);
-    L.plan = off;
-    off = align_up(off + sizeof(Plan), 1024);
-    L.wq = off;
-    off = align_up(off + sizeof(float) * (size_t)R * kHeads, 1024);
-    L.q8 = off;
-    off = align_up(off + (size_t)2 * R * kHeads * kDim, 1024);
+    L.status = 0;
     L.score_stride = (max_len + 3) / 4 * 4;
     if (L.score_stride < 4) L.score_stride = 4;
-    L.scores = off;
-    if (with_scores) off = align_up(off + sizeof(float) * (size_t)R * (size_t)L.score_stride, 1024);
-    L.end = off;
+    L.scores = 1024;
+    L.end = with_scores ? align_up(L.scores + sizeof(float) * (size_t)R * (size_t)L.score_stride, 1024) : 1024;
     return L;
 }
 
@@ -94,9 +67,7 @@ struct ScoreArgs {
     int num_sms;
 };
 
-cudaError_t launch_prep(const ScoreArgs& a);
-cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map,
-                         const CUtensorMap& q_map);
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);
 
 struct SelectArgs {
     const float* scores;
@@ -107,6 +78,7 @@ struct SelectArgs {
     int32_t* indices;
     uint32_t* status;     // may be null
     int64_t max_len;      // bound on row lengths (launch shape)
+    int64_t len_cap;      // rows longer than this are cut to it (and reported)
     cudaStream_t stream;
 };
 

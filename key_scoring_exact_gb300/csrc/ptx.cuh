@@ -123,6 +123,10 @@ IDX_DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* ba
         : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tensor-core operands, bulk copies).
+IDX_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 IDX_DEVI void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

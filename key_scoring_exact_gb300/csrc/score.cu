@@ -7,33 +7,49 @@
 //     s[row, key] = scale[key] * sum_h w'[row, h] * max(D[key, (row, h)], 0)
 //
 // which is the indexer score sum_h w * ReLU(q . (k * scale)) once the key's
-// scale (>= 0) and the query's power-of-two factor are taken out of the ReLU
-// (see prep.cu).  Every key of a request is read from HBM once per group, as
-// "sgl-amd-mono-upstream PR 18" (GLM-5.3 indexer launch), section
-// "Modifications / 2. A request's rows scored together" asks; its LDS batches
-// of whole pages become TMA loads of whole 64-token pages into a ring of
-// shared-memory stages.
+// scale (>= 0) and the query's power-of-two factor are taken out of the ReLU.
+// Every key of a request is read from HBM once per group, as "sgl-amd-mono-
+// upstream PR 18" (GLM-5.3 indexer launch), section "Modifications / 2. A
+// request's rows scored together" asks; its LDS batches of whole pages become
+// TMA loads of whole 64-token pages into a ring of shared-memory stages.
+//
+// The query on FP8 tensor cores.  A bf16 query element has 8 significant bits
+// and E4M3 only 4, so each (row, head) vector is scaled by a power of two 2^e
+// that brings its largest element into [128, 256) and split exactly into two
+// E4M3 terms: x * 2^e = hi + lo, hi = RN_e4m3(x * 2^e), lo = x * 2^e - hi.
+// For every element whose scaled magnitude is at least 2^-2, lo is a multiple
+// of the element's bf16 ulp no larger than 8 ulps, so it is an E4M3 value and
+// the split is exact; smaller elements lose at most 2^-10 (scaled) to E4M3's
+// subnormal grid -- below 8e-6 of the head's largest element.  The two terms
+// accumulate into one TMEM accumulator, and 2^-e > 0 commutes with the ReLU,
+// so it is folded into the head weight: w'[r,h] = w[r,h] * 2^-e[r,h].  An
+// E4M3 query is used as is (hi = q, no lo term, w' = w).
 //
 // Keys sit on the MMA's M dimension (128 lanes of TMEM = 128 keys) and the
 // group's (row, head) pairs on N (<= 256 columns), so the epilogue reads one
 // key per thread and reduces over heads inside the thread: no cross-lane sums,
 // and each warp stores 32 consecutive scores of a row.
 //
-// Warp roles (one CTA per SM, persistent over a contiguous range of tiles):
-//   warp 0     TMA producer: the group's query (E4M3 hi/lo parts), then per
-//              tile two key pages (TMA, 128-byte swizzle) + their scales
-//              (bulk copy) into stage s of an 8-stage ring.
+// One launch, one CTA per SM, persistent over a contiguous range of tiles:
+//   all        build the plan in shared memory: consecutive rows of one
+//              request form groups of at most four rows, each group's keys
+//              are cut into 128-key tiles numbered as work items.
+//   warp 0     TMA producer: the whole warp fetches block-table entries (one
+//              page per lane), lane 0 issues per tile two key pages (TMA,
+//              128-byte swizzle) + their scales (bulk copy) into stage s of a
+//              7-stage ring.
 //   warp 1     TMEM allocator and MMA issuer: 4 (E4M3 query) or 8 (bf16 query,
 //              hi and lo terms) kind::f8f6f4 MMAs of K = 32 per tile into one
 //              of two TMEM accumulators.
-//   warps 2-17 epilogue, one (row, TMEM lane quadrant) per warp: tcgen05.ld
-//              the row's 64 head columns (two halves), ReLU, head-weighted sum
-//              (packed f32x2 FMAs), times the key scale, masked coalesced f32
-//              stores; then the accumulator goes back to the MMA issuer.
-//
-// The launch is a programmatic dependent of the prep kernel: barrier set-up,
-// TMEM allocation and descriptor prefetch overlap the prep kernel's tail, and
-// nothing it wrote is read before griddepcontrol.wait.
+//   warps 2-17 epilogue.  At each group they first split the group's query
+//              into the swizzled shared-memory operand (while the producer
+//              already streams keys), then per tile one (row, TMEM lane
+//              quadrant) per warp: tcgen05.ld the row's 64 head columns, ReLU,
+//              head-weighted sum (packed f32x2 FMAs), times the key scale,
+//              masked coalesced f32 stores.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -41,7 +57,7 @@ namespace idx {
 
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 7;
 constexpr int kEpiWarps = 16;                              // 4 rows x 4 TMEM lane quadrants
 constexpr int kScoreThreads = 64 + kEpiWarps * 32;         // 576
 constexpr uint32_t kQRows = kGroupRows * kHeads;           // 256
@@ -52,58 +68,215 @@ constexpr uint32_t kStageBytes = kTileKeys * kDim;         // 16 KB
 constexpr uint32_t kStageScaleBytes = kTileKeys * 4;       // 512 B
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr int kPlanCacheGroups = 256;                      // plan entries kept in shared memory
-constexpr int kPlanCacheRows = kMaxRows;
 
 constexpr uint32_t kOffQHi = 0;
 constexpr uint32_t kOffQLo = kOffQHi + kQPartBytes;
 constexpr uint32_t kOffStages = kOffQLo + kQPartBytes;
 constexpr uint32_t kOffScales = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffWq = kOffScales + kStages * kStageScaleBytes;
-constexpr uint32_t kOffPlan = kOffWq + kEpiWarps * kHeads * 4;
-constexpr uint32_t kPlanInts = 5 * kPlanCacheGroups + 1 + kPlanCacheRows;
-constexpr uint32_t kOffBars = kOffPlan + kPlanInts * 4 + 4;
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 3;
+constexpr uint32_t kOffWq = kOffScales + kStages * kStageScaleBytes;   // [2][256] f32, by group parity
+constexpr uint32_t kOffPlan = kOffWq + 2 * kQRows * 4;
+// plan: item[kMaxRows+1], req, r0, nr, len [kMaxRows] each, row_len[kMaxRows], gid[kMaxRows]
+constexpr uint32_t kPlanInts = (kMaxRows + 1) + 4 * kMaxRows + 2 * kMaxRows;
+constexpr uint32_t kOffBars = ((kOffPlan + kPlanInts * 4) + 7) & ~7u;
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 2;
 constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStages % 1024 == 0 && kOffQLo % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-static_assert(kOffBars % 8 == 0, "mbarrier alignment");
 
 struct ScoreParams {
-    const Plan* plan;
-    const float* wq;
+    int qtype;
+    const void* q;
+    const float* head_w;
+    const int32_t* seq_lens;
+    const int32_t* row_req;
+    int R;
+    int64_t len_cap;  // rows are cut to this many keys (block table and score buffer)
     const float* k_scale;
     const int32_t* block_table;
     int64_t pool_pages;
     int max_pages;
-    int R;
-    int two_terms;  // 1: bf16 query split into hi + lo E4M3 terms
     float* scores;
     int64_t score_stride;
     uint32_t* status;
 };
 
-// The plan, read from shared memory when it fits there, else from global.
-struct PlanView {
-    const int* item;  // [n_groups + 1]
-    const int* req;
-    const int* r0;
-    const int* nr;
-    const int* len;
-    const int* row_len;
-    int n_groups;
-    // The group that holds work item `it`: the last g with item[g] <= it.
-    __device__ __forceinline__ int find(int it) const {
-        int lo = 0, hi = n_groups;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (item[mid] <= it) lo = mid; else hi = mid;
-        }
-        return lo;
-    }
+struct PlanSmem {
+    int* item;     // [n_groups + 1] first work item of each group
+    int* req;      // request of each group
+    int* r0;       // first row of each group
+    int* nr;       // rows in each group
+    int* len;      // longest row of each group
+    int* row_len;  // [R] clamped row lengths
+    int* gid;      // [R] group of each row (scratch)
 };
+
+__device__ __forceinline__ int find_group(const PlanSmem& pl, int n_groups, int it) {
+    int lo = 0, hi = n_groups;  // item[lo] <= it < item[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pl.item[mid] <= it) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Warp 0: group rows r and r-1 when they have the same request, at most
+// kGroupRows rows a group; tiles of each group numbered in one sequence.
+__device__ void build_plan(const ScoreParams& p, const PlanSmem& pl, int* n_groups_out, int* n_items_out) {
+    const int lane = threadIdx.x & 31;
+    const unsigned full = 0xFFFFFFFFu;
+    const int R = p.R;
+    int carry_seg = 0, carry_req = -1, n_groups = 0;
+    bool bad = false;
+    for (int base = 0; base < R; base += 32) {
+        const int r = base + lane;
+        const bool valid = r < R;
+        const int req = valid ? p.row_req[r] : -1;
+        int len = valid ? p.seq_lens[r] : 0;
+        if (valid) {
+            if (len < 0 || (int64_t)len > p.len_cap || req < 0) bad = true;
+            len = len < 0 ? 0 : ((int64_t)len > p.len_cap ? (int)p.len_cap : len);
+            if (req < 0) len = 0;
+            pl.row_len[r] = len;
+        }
+        int prev_req = __shfl_up_sync(full, req, 1);
+        if (lane == 0) prev_req = carry_req;
+        const bool seg_start = valid && (r == 0 || req != prev_req);
+        const unsigned upto = full >> (31 - lane);  // lanes 0..lane
+        const unsigned starts = __ballot_sync(full, seg_start) & upto;
+        const int seg = starts ? base + (31 - __clz(starts)) : carry_seg;
+        const bool gstart = valid && ((r - seg) % kGroupRows == 0);
+        const unsigned gs = __ballot_sync(full, gstart);
+        const int gid = n_groups + __popc(gs & upto) - 1;
+        if (valid) pl.gid[r] = gid;
+        if (gstart) {
+            pl.req[gid] = req;
+            pl.r0[gid] = r;
+        }
+        n_groups += __popc(gs);
+        carry_seg = __shfl_sync(full, seg, 31);
+        carry_req = __shfl_sync(full, req, 31);
+    }
+    __syncwarp();
+    if (blockIdx.x == 0 && __any_sync(full, bad) && lane == 0) record_status(p.status, kStatusBounds);
+    int item = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+        const int g = base + lane;
+        int ntiles = 0;
+        if (g < n_groups) {
+            const int r0 = pl.r0[g];
+            int nr = 0, glen = 0;
+            for (int i = 0; i < kGroupRows && r0 + i < R; ++i) {
+                if (pl.gid[r0 + i] != g) break;
+                ++nr;
+                glen = max(glen, pl.row_len[r0 + i]);
+            }
+            pl.nr[g] = nr;
+            pl.len[g] = glen;
+            ntiles = (glen + kTileKeys - 1) / kTileKeys;
+        }
+        int incl = ntiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (g < n_groups) pl.item[g] = item + incl - ntiles;
+        item += __shfl_sync(full, incl, 31);
+    }
+    if (lane == 0) {
+        pl.item[n_groups] = item;
+        *n_groups_out = n_groups;
+        *n_items_out = item;
+    }
+}
+
+__device__ __forceinline__ uint16_t to_e4m3_pair(float a, float b) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint16_t codes, int which) {
+    __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+    __half_raw h;
+    h.x = which ? h2.y : h2.x;
+    return __half2float(__half(h));
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]: exact 2^e
+    return __int_as_float((e + 127) << 23);
+}
+
+// Byte offset of 4-byte group `lane` of B-operand row n in the K-major
+// 128-byte-swizzle layout (8-row atoms of 1024 bytes, 16-byte chunks XOR row).
+__device__ __forceinline__ uint32_t swz_off(int n, int lane) {
+    return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((((lane >> 2) ^ (n & 7)) & 7) << 4) + ((lane & 3) << 2));
+}
+
+// The epilogue warps split the query of a group (rows r0 .. r0+nr-1) into
+// the hi / lo operand buffers and write w' for each (row, head).
+__device__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t* q_hi, uint8_t* q_lo,
+                                  float* wq, int e, int lane) {
+    const int pairs = nr * kHeads;
+    if (p.qtype == IDX_Q_E4M3) {
+        for (int pp = e; pp < pairs; pp += kEpiWarps) {
+            const int64_t src = (int64_t)r0 * kHeads + pp;
+            const uint32_t v = reinterpret_cast<const uint32_t*>(p.q)[src * 32 + lane];
+            *reinterpret_cast<uint32_t*>(q_hi + swz_off(pp, lane)) = v;
+            if (lane == 0) wq[pp] = p.head_w[src];
+        }
+        return;
+    }
+    constexpr int kBatch = 8;  // pairs whose loads are in flight together
+    for (int p0 = e; p0 < pairs; p0 += kEpiWarps * kBatch) {
+        uint2 raw[kBatch];
+        float wv[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int pp = p0 + b * kEpiWarps;
+            raw[b] = make_uint2(0, 0);
+            wv[b] = 0.0f;
+            if (pp < pairs) {
+                const int64_t src = (int64_t)r0 * kHeads + pp;
+                raw[b] = reinterpret_cast<const uint2*>(p.q)[src * 32 + lane];
+                wv[b] = p.head_w[src];
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int pp = p0 + b * kEpiWarps;
+            if (pp >= pairs) break;  // warp-uniform
+            float x[4];
+            x[0] = __uint_as_float(raw[b].x << 16);
+            x[1] = __uint_as_float(raw[b].x & 0xFFFF0000u);
+            x[2] = __uint_as_float(raw[b].y << 16);
+            x[3] = __uint_as_float(raw[b].y & 0xFFFF0000u);
+            // Largest exponent field of the 128 elements (one warp reduction);
+            // the largest element lies in [2^(E-127), 2^(E-126)).
+            const uint32_t e01 = max((raw[b].x >> 7) & 0xFFu, (raw[b].x >> 23) & 0xFFu);
+            const uint32_t e23 = max((raw[b].y >> 7) & 0xFFu, (raw[b].y >> 23) & 0xFFu);
+            const int emax = (int)__reduce_max_sync(0xFFFFFFFFu, max(e01, e23));
+            // 2^ex brings the largest element into [128, 256) (<= 448).
+            const int ex = max(-126, min(126, 134 - emax));
+            const float sc = pow2f(ex);
+            float xs[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[i] = x[i] * sc;
+            const uint16_t h01 = to_e4m3_pair(xs[0], xs[1]);
+            const uint16_t h23 = to_e4m3_pair(xs[2], xs[3]);
+            lo[0] = __fsub_rn(xs[0], e4m3_to_float(h01, 0));
+            lo[1] = __fsub_rn(xs[1], e4m3_to_float(h01, 1));
+            lo[2] = __fsub_rn(xs[2], e4m3_to_float(h23, 0));
+            lo[3] = __fsub_rn(xs[3], e4m3_to_float(h23, 1));
+            const uint16_t l01 = to_e4m3_pair(lo[0], lo[1]);
+            const uint16_t l23 = to_e4m3_pair(lo[2], lo[3]);
+            const uint32_t off = swz_off(pp, lane);
+            *reinterpret_cast<uint32_t*>(q_hi + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
+            *reinterpret_cast<uint32_t*>(q_lo + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
+            if (lane == 0) wq[pp] = wv[b] * pow2f(-ex);
+        }
+    }
+}
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
     uint64_t r;
@@ -122,8 +295,7 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
-k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap q_map,
-        const ScoreParams p) {
+k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_hi = smem + kOffQHi;
@@ -137,15 +309,22 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
     uint64_t* empty = bars + kStages;         // [kStages] MMAs done (seen by the epilogue), scales read
     uint64_t* tfull = bars + 2 * kStages;     // [2] accumulator ready
     uint64_t* tempty = tfull + 2;             // [2] accumulator drained
-    uint64_t* qfull = tempty + 2;             // group query landed
-    uint64_t* qempty = qfull + 1;             // MMAs on the group query done
-    uint64_t* drain = qempty + 1;             // final MMA completion
+    uint64_t* qfull = tempty + 2;             // the group's query operand written
+    uint64_t* drain = qfull + 1;              // final MMA completion
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    int* counts = reinterpret_cast<int*>(smem + kOffMisc + 8);  // n_groups, n_items
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    PlanSmem pl;
+    pl.item = plan_s;
+    pl.req = pl.item + kMaxRows + 1;
+    pl.r0 = pl.req + kMaxRows;
+    pl.nr = pl.r0 + kMaxRows;
+    pl.len = pl.nr + kMaxRows;
+    pl.row_len = pl.len + kMaxRows;
+    pl.gid = pl.row_len + kMaxRows;
 
-    // ---- set-up that needs nothing from the prep kernel --------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -155,63 +334,22 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], kEpiWarps);
         }
-        mbar_init(qfull, 1);
-        mbar_init(qempty, 1);
+        mbar_init(qfull, kEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&keys_map);
-        prefetch_tensormap(&q_map);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    pdl_wait();               // the prep kernel's plan and query are complete and visible
-    pdl_launch_dependents();  // the selection may be scheduled as SMs free up
-
-    // ---- the plan: one coalesced copy into shared memory ------------------
-    const Plan* plan = p.plan;
-    const int n_items = plan->n_items;
-    const int n_groups = plan->n_groups;
-    PlanView pv;
-    pv.n_groups = n_groups;
-    if (n_groups <= kPlanCacheGroups) {
-        int* it_s = plan_s;
-        int* rq_s = it_s + kPlanCacheGroups + 1;
-        int* r0_s = rq_s + kPlanCacheGroups;
-        int* nr_s = r0_s + kPlanCacheGroups;
-        int* ln_s = nr_s + kPlanCacheGroups;
-        for (int i = threadIdx.x; i <= n_groups; i += kScoreThreads) {
-            it_s[i] = plan->g_item[i];
-            if (i < n_groups) {
-                rq_s[i] = plan->g_req[i];
-                r0_s[i] = plan->g_r0[i];
-                nr_s[i] = plan->g_nr[i];
-                ln_s[i] = plan->g_len[i];
-            }
-        }
-        pv.item = it_s;
-        pv.req = rq_s;
-        pv.r0 = r0_s;
-        pv.nr = nr_s;
-        pv.len = ln_s;
-    } else {
-        pv.item = plan->g_item;
-        pv.req = plan->g_req;
-        pv.r0 = plan->g_r0;
-        pv.nr = plan->g_nr;
-        pv.len = plan->g_len;
-    }
-    {
-        int* rl_s = plan_s + 5 * kPlanCacheGroups + 1;
-        for (int i = threadIdx.x; i < p.R && i < kPlanCacheRows; i += kScoreThreads) rl_s[i] = plan->row_len[i];
-        pv.row_len = p.R <= kPlanCacheRows ? rl_s : plan->row_len;
-    }
+    if (warp == 0) build_plan(p, pl, &counts[0], &counts[1]);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    const int n_groups = counts[0], n_items = counts[1];
     const int it0 = (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
     const int it1 = (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
     const bool has_work = it0 < it1 && n_groups >= 1;
@@ -223,38 +361,15 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
         // The whole warp fetches block-table entries, one page per lane and
         // up to 16 tiles at a time, so the page ids of a batch arrive in one
         // round trip; lane 0 waits on the ring and issues the copies.
-        int g = pv.find(it0), cur_g = -1, qi = 0, issued = 0;
-        int req = 0, npages = 0, gbeg = 0, gend = 0;
+        int g = find_group(pl, n_groups, it0), issued = 0;
         bool stop = false;
         int it = it0;
         while (it < it1 && !stop) {
-            while (g + 1 < n_groups && it >= pv.item[g + 1]) ++g;
-            if (g != cur_g) {
-                req = pv.req[g];
-                npages = (pv.len[g] + kPage - 1) / kPage;
-                gbeg = pv.item[g];
-                gend = pv.item[g + 1];
-                if (lane == 0) {
-                    if (!bounded_wait(qempty, (qi & 1) ^ 1, abort_flag)) {
-                        stop = true;
-                    } else {
-                        const int r0 = pv.r0[g], nr = pv.nr[g];
-                        mbar_arrive_expect_tx(qfull, (uint32_t)nr * kPageKeyBytes * (p.two_terms ? 2u : 1u));
-                        for (int i = 0; i < nr; ++i) {
-                            tma_load_2d(q_hi + i * kPageKeyBytes, &q_map, qfull, 0, (r0 + i) * kHeads);
-                            if (p.two_terms)
-                                tma_load_2d(q_lo + i * kPageKeyBytes, &q_map, qfull, 0,
-                                            (p.R + r0 + i) * kHeads);
-                        }
-                        ++qi;
-                    }
-                }
-                stop = __shfl_sync(0xFFFFFFFFu, stop ? 1 : 0, 0) != 0;
-                cur_g = g;
-                if (stop) break;
-            }
-            const int nb = min(16, min(it1, gend) - it);
-            const int t0 = it - gbeg;
+            while (g + 1 < n_groups && it >= pl.item[g + 1]) ++g;
+            const int req = pl.req[g];
+            const int npages = (pl.len[g] + kPage - 1) / kPage;
+            const int nb = min(16, min(it1, pl.item[g + 1]) - it);
+            const int t0 = it - pl.item[g];
             int id = -1;
             if (lane < 2 * nb) {
                 const int pidx = 2 * t0 + lane;
@@ -299,32 +414,28 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
             int dummy = 0;
             const int first = issued > kStages ? issued - kStages : 0;
             for (int j = first; j < issued; ++j) bounded_wait(&full[j % kStages], (j / kStages) & 1, &dummy);
-            if (qi > 0) bounded_wait(qfull, (qi - 1) & 1, &dummy);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t a0 = smem_u32(stages), bh = smem_u32(q_hi), bl = smem_u32(q_lo);
-            const int nmma = p.two_terms ? 8 : 4;
-            int g = pv.find(it0), qi = 0;
-            int gend = pv.item[g + 1];  // first work item past the current group
+            const int nmma = p.qtype == IDX_Q_BF16 ? 8 : 4;
+            int g = find_group(pl, n_groups, it0), qi = 0;
+            int gend = -1;  // first work item past the current group
             uint32_t idesc = 0;
-            bool ok = true;
             for (int it = it0, li = 0; it < it1; ++it, ++li) {
-                if (it == it0 || it >= gend) {
-                    if (it != it0) {
-                        mma_commit(qempty);  // the previous group's query may be replaced
-                        while (g + 1 < n_groups && it >= pv.item[g + 1]) ++g;
-                        gend = pv.item[g + 1];
-                    }
-                    if (!bounded_wait(qfull, qi & 1, abort_flag)) { ok = false; break; }
+                if (it >= gend) {
+                    while (g + 1 < n_groups && it >= pl.item[g + 1]) ++g;
+                    gend = pl.item[g + 1];
+                    // the epilogue has written this group's query operand
+                    if (!bounded_wait(qfull, qi & 1, abort_flag)) break;
                     tc_fence_after_sync();
-                    idesc = idesc_e4m3_f32(128, (uint32_t)pv.nr[g] * kHeads);
+                    idesc = idesc_e4m3_f32(128, (uint32_t)pl.nr[g] * kHeads);
                     ++qi;
                 }
-                if (!bounded_wait(&tempty[li & 1], ((li >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!bounded_wait(&tempty[li & 1], ((li >> 1) & 1) ^ 1, abort_flag)) break;
                 tc_fence_after_sync();
-                if (!bounded_wait(&full[li % kStages], (li / kStages) & 1, abort_flag)) { ok = false; break; }
+                if (!bounded_wait(&full[li % kStages], (li / kStages) & 1, abort_flag)) break;
                 const uint32_t d = tmem_base + (uint32_t)(li & 1) * kAccCols;
                 const uint32_t a = a0 + (uint32_t)(li % kStages) * kStageBytes;
                 for (int k = 0; k < nmma; ++k) {  // K slice k % 4 of the hi (k < 4) or lo term
@@ -334,7 +445,6 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
                 }
                 mma_commit(&tfull[li & 1]);
             }
-            (void)ok;
             // Every MMA issued here must finish before TMEM is released.
             int dummy = 0;
             mma_commit(drain);
@@ -346,23 +456,28 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
         const int quad = warp & 3;         // TMEM lanes this warp may read
         const int rr = e >> 2;             // the group row this warp reduces
         const int key = quad * 32 + lane;  // key of the tile this thread owns
-        float* w = wq_s + e * kHeads;      // this warp's copy of its row's head weights
-        int g = pv.find(it0), li = 0;
+        int g = find_group(pl, n_groups, it0), li = 0, qi = 0;
         int gend = -1, gbeg = 0, r0 = 0, nr = 0, rlen = 0;
+        const float* w = wq_s;
         for (int it = it0; it < it1; ++it, ++li) {
             if (it >= gend) {
-                while (g + 1 < n_groups && it >= pv.item[g + 1]) ++g;
-                gbeg = pv.item[g];
-                gend = pv.item[g + 1];
+                // A new group.  Every MMA that read the previous group's query has
+                // completed (this warp waited for the last one's accumulator), so
+                // the operand can be rewritten.
+                while (g + 1 < n_groups && it >= pl.item[g + 1]) ++g;
+                gbeg = pl.item[g];
+                gend = pl.item[g + 1];
+                r0 = pl.r0[g];
+                nr = pl.nr[g];
+                rlen = rr < nr ? pl.row_len[r0 + rr] : 0;
+                float* wbuf = wq_s + (qi & 1) * kQRows;
+                split_group_query(p, r0, nr, q_hi, q_lo, wbuf, e, lane);
+                fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's operand reads
                 __syncwarp();
-                r0 = pv.r0[g];
-                nr = pv.nr[g];
-                rlen = rr < nr ? pv.row_len[r0 + rr] : 0;
-                if (rr < nr) {
-                    w[lane] = p.wq[(int64_t)(r0 + rr) * kHeads + lane];
-                    w[32 + lane] = p.wq[(int64_t)(r0 + rr) * kHeads + 32 + lane];
-                }
-                __syncwarp();
+                if (lane == 0) mbar_arrive(qfull);
+                if (!bounded_wait(qfull, qi & 1, abort_flag)) break;  // every warp's w' is written
+                w = wbuf + rr * kHeads;
+                ++qi;
             }
             const int s = li % kStages, acc = li & 1;
             if (!bounded_wait(&tfull[acc], (li >> 1) & 1, abort_flag)) break;
@@ -415,7 +530,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CU
 
 }  // namespace
 
-cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map, const CUtensorMap& q_map) {
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     static int configured_device = -1;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -426,28 +541,22 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map, const 
         configured_device = dev;
     }
     ScoreParams p;
-    p.plan = reinterpret_cast<const Plan*>(a.ws + a.L.plan);
-    p.wq = reinterpret_cast<const float*>(a.ws + a.L.wq);
+    p.qtype = a.qtype;
+    p.q = a.q;
+    p.head_w = a.head_w;
+    p.seq_lens = a.seq_lens;
+    p.row_req = a.row_req;
+    p.R = a.R;
+    p.len_cap = a.len_bound < (int64_t)a.max_pages * kPage ? a.len_bound : (int64_t)a.max_pages * kPage;
     p.k_scale = a.k_scale;
     p.block_table = a.block_table;
     p.pool_pages = a.pool_pages;
     p.max_pages = a.max_pages;
-    p.R = a.R;
-    p.two_terms = a.qtype == IDX_Q_BF16 ? 1 : 0;
     p.scores = a.scores;
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.num_sms, 1, 1);
-    cfg.blockDim = dim3(kScoreThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_score, keys_map, q_map, p);
+    k_score<<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
+    return cudaGetLastError();
 }
 
 }  // namespace idx

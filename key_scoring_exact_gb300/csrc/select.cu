@@ -17,13 +17,21 @@
 //  * Digits of 11, 11 and 10 bits: three rounds give the exact k-th largest
 //    image T and the number kr of keys equal to T that the list takes.
 //  * Histograms are built in shared memory with warp-aggregated atomics (the
-//    lanes sharing a hot digit add once), then added into CTA 0's copy with
-//    distributed-shared-memory reductions; after one hardware cluster barrier
-//    every slice reads the totals back and scans them.  No slice spins on
-//    another; every wait is a cluster barrier.
-//  * Each slice then counts its keys above / at T; the counts of earlier
-//    slices give its output offsets, and positions are written in order:
-//    keys above T first, then ties, each in ascending position.
+//    lanes sharing a hot digit add once); each slice then adds its non-zero
+//    bins into every slice's own totals with distributed-shared-memory
+//    reductions, so after one hardware cluster barrier each slice scans its
+//    local totals.  No slice spins on another; every wait is a cluster
+//    barrier.
+//  * After the first round, when the bin that holds the k-th key has at most
+//    8,192 keys across the row, every slice appends its keys of that bin to a
+//    candidate array in CTA 0 (a remote atomic reserves the room), and CTA 0
+//    alone runs the last two rounds on them, then writes T and kr into every
+//    slice: two rounds without a cluster barrier each.  A fuller bin takes
+//    the last two rounds on all slices as above.
+//  * Each slice then counts its keys above / at T and adds the counts to every
+//    later slice; after one more barrier the counts of earlier slices give its
+//    output offsets, and positions are written in order: keys above T first,
+//    then ties, each in ascending position.
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -37,6 +45,7 @@ constexpr int kBinsMax = 2048;
 constexpr int kSliceTarget = 4096;  // keys per slice the launcher aims for
 constexpr int kSliceCapMax = 32768; // keys one slice can hold (128 KB of shared memory)
 constexpr int kMaxChunks = kSliceCapMax / (4 * kThreads);
+constexpr int kCandCap = 8192;      // candidates CTA 0 resolves alone after the first round
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -62,13 +71,13 @@ __device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
 __device__ __forceinline__ void red_add_remote(uint32_t addr, uint32_t v) {
     asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_remote(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
 __device__ __forceinline__ void st_remote(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_remote(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ uint32_t radix_key(float x) {
@@ -93,77 +102,26 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool hit, uint32_t d, int 
 
 struct Shared {
     uint32_t hloc[kBinsMax];             // this slice's histogram of the round
-    uint32_t htot[3][kBinsMax];          // cluster totals (CTA 0's copy is the one used)
-    uint32_t ctot[3][kBinsMax / 32];     // coarse totals: 32 fine bins each (CTA 0's copy)
-    uint32_t cloc[kBinsMax / 32];        // this slice's coarse histogram
-    uint32_t cnt[2][kMaxCluster];        // per-slice counts above / at T (CTA 0's copy)
-    uint32_t pick[2];
+    uint32_t htot[3][kBinsMax];          // totals of every slice, one buffer per round
+    uint32_t cnt[2][kMaxCluster];        // counts above / at T of every earlier slice
+    uint32_t wsum[kWarps];
+    uint32_t pick[3];                    // digit, keys above it, keys in it
+    uint32_t cand_n;                     // candidates gathered so far (CTA 0's copy)
+    uint32_t bcast[2];                   // T and kr, written by CTA 0 into every slice
     uint32_t woff[2][kMaxChunks * kWarps];  // per (chunk, warp) counts, then offsets
     uint32_t tot[2];                     // this slice's counts above / at T
     uint32_t base[2];                    // counts of the earlier slices
 };
 
-// Warp 0: find the digit holding rank kr (counting from the largest digit)
-// from nc coarse totals (32 digits each) and, inside the chosen coarse bin,
-// its 32 fine totals.  coarse(i) / fine(i) read totals; the result goes to
-// S.pick (digit, keys above it).
-template <typename Coarse, typename Fine>
-__device__ __forceinline__ void pick_digit_warp(int nc, uint32_t kr, Shared& S, int lane, Coarse coarse,
-                                                Fine fine) {
-    const int cpl = nc / 32;  // coarse bins per lane: 2 or 1; lane L holds nc-1-(L*cpl+q)
-    uint32_t cv[2] = {0u, 0u}, s = 0;
-    for (int q = 0; q < cpl; ++q) {
-        cv[q] = coarse(nc - 1 - (lane * cpl + q));
-        s += cv[q];
-    }
-    uint32_t incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += v;
-    }
-    uint32_t above = incl - s;
-    int cb = -1;
-    uint32_t cabove = 0;
-    for (int q = 0; q < cpl; ++q) {
-        if (above < kr && above + cv[q] >= kr) {
-            cb = nc - 1 - (lane * cpl + q);
-            cabove = above;
-        }
-        above += cv[q];
-    }
-    const uint32_t who = __ballot_sync(kFull, cb >= 0);
-    const int src = who ? __ffs(who) - 1 : 0;
-    cb = __shfl_sync(kFull, cb, src);
-    cabove = __shfl_sync(kFull, cabove, src);
-    if (cb < 0) cb = 0;  // unreachable when kr <= the keys under the prefix
-    // fine bins of coarse bin cb, descending: lane L holds digit cb*32 + 31 - L
-    const int d = cb * 32 + 31 - lane;
-    const uint32_t f = fine(d);
-    uint32_t finc = f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(kFull, finc, o);
-        if (lane >= o) finc += v;
-    }
-    const uint32_t fab = cabove + finc - f;
-    if (fab < kr && fab + f >= kr) {
-        S.pick[0] = (uint32_t)d;
-        S.pick[1] = fab;
-    }
-}
-
 // One digit round (digit = (key >> shift) & (nb - 1)) over the slice's keys
 // whose bits above the digit equal `prefix` under `mask`.  Leaves the digit
-// holding rank kr and the count above it in S.pick.  One copy of this code
-// serves all rounds.
+// holding rank kr (counted from the largest digit) and the number of keys
+// above it in S.pick.  One copy of this code serves all rounds.
 __device__ __noinline__ void digit_round(const uint32_t* __restrict__ keys, int cnt, uint32_t prefix,
                                          uint32_t mask, int shift, int nb, uint32_t kr, bool single, int r,
-                                         Shared& S) {
+                                         int nslices, Shared& S) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bpt = nb / kThreads;  // fine bins per thread: 4 or 2
-    const int tpc = 32 / bpt;       // threads per coarse bin: 8 or 16
-    for (int q = 0; q < bpt; ++q) S.hloc[tid * bpt + q] = 0;
+    for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
     __syncthreads();
     const uint32_t dm = (uint32_t)nb - 1;
     const int n4 = (cnt + 3) >> 2;
@@ -179,37 +137,60 @@ __device__ __noinline__ void digit_round(const uint32_t* __restrict__ keys, int 
         hist_add(S.hloc, i + 3 < cnt && (u.w & mask) == prefix, (u.w >> shift) & dm, lane);
     }
     __syncthreads();
-    // coarse sums of 32 fine bins (tpc consecutive threads)
-    uint32_t fv[4] = {0u, 0u, 0u, 0u}, part = 0;
-    for (int q = 0; q < bpt; ++q) {
-        fv[q] = S.hloc[tid * bpt + q];
-        part += fv[q];
-    }
-    for (int o = 1; o < tpc; o <<= 1) part += __shfl_xor_sync(kFull, part, o);
-    if (single) {
-        if (tid % tpc == 0) S.cloc[tid / tpc] = part;
-        __syncthreads();
-        if (warp == 0)
-            pick_digit_warp(nb / 32, kr, S, lane, [&](int i) { return S.cloc[i]; },
-                            [&](int i) { return S.hloc[i]; });
-    } else {
-        const uint32_t rf = map_rank(&S.htot[r][0], 0), rc = map_rank(&S.ctot[r][0], 0);
-        for (int q = 0; q < bpt; ++q)
-            if (fv[q]) red_add_remote(rf + 4 * (tid * bpt + q), fv[q]);
-        if (tid % tpc == 0 && part) red_add_remote(rc + 4 * (tid / tpc), part);
+    const uint32_t* totals = S.hloc;
+    if (!single) {
+        // every non-zero bin into every slice's totals for this round
+        for (int b = tid; b < nb; b += kThreads) {
+            const uint32_t v = S.hloc[b];
+            if (v)
+                for (int t = 0; t < nslices; ++t) red_add_remote(map_rank(&S.htot[r][b], (uint32_t)t), v);
+        }
         cluster_arrive();
         cluster_wait();
-        if (warp == 0)
-            pick_digit_warp(nb / 32, kr, S, lane, [&](int i) { return ld_remote(rc + 4 * i); },
-                            [&](int i) { return ld_remote(rf + 4 * i); });
+        totals = S.htot[r];
+    }
+    // Scan in descending digit order: thread tid holds digits nb-1-(bpt*tid+q).
+    const int bpt = nb / kThreads;  // 2 or 1
+    uint32_t tv[2] = {0u, 0u}, sum = 0;
+    for (int q = 0; q < bpt; ++q) {
+        tv[q] = totals[nb - 1 - (bpt * tid + q)];
+        sum += tv[q];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the warp totals
+        const uint32_t wv = S.wsum[lane];
+        uint32_t wi = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, wi, o);
+            if (lane >= o) wi += x;
+        }
+        S.wsum[lane] = wi - wv;
+    }
+    __syncthreads();
+    uint32_t above = S.wsum[warp] + incl - sum;
+    for (int q = 0; q < bpt; ++q) {
+        if (above < kr && above + tv[q] >= kr) {
+            S.pick[0] = (uint32_t)(nb - 1 - (bpt * tid + q));
+            S.pick[1] = above;
+            S.pick[2] = tv[q];
+        }
+        above += tv[q];
     }
     __syncthreads();
 }
 
 template <int CL>
 __global__ void __launch_bounds__(kThreads)
-k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ row_lens,
-         int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap) {
+k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __restrict__ row_lens,
+         int64_t stride, int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap) {
     extern __shared__ __align__(16) uint32_t keys_s[];  // slice_cap radix keys
     __shared__ Shared S;
     const uint32_t c = cluster_ctarank();
@@ -217,9 +198,9 @@ k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __rest
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     int64_t n = row_lens[row];
-    if (n < 0 || n > stride) {
+    if (n < 0 || n > len_cap) {
         if (c == 0 && tid == 0) record_status(status, kStatusBounds);
-        n = n < 0 ? 0 : stride;
+        n = n < 0 ? 0 : len_cap;
     }
     if (n > (int64_t)CL * slice_cap) {  // the launcher sizes slice_cap for the longest row
         if (c == 0 && tid == 0) record_status(status, kStatusBounds);
@@ -245,13 +226,12 @@ k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __rest
     const float* src = scores + (int64_t)row * stride + start;
 
     if (!single) {
-        if (c == 0) {
-            uint32_t* h = &S.htot[0][0];
-            for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
-            uint32_t* hc = &S.ctot[0][0];
-            for (int i = tid; i < 3 * (kBinsMax / 32); i += kThreads) hc[i] = 0;
-        }
-        cluster_arrive();  // CTA 0's zeroed totals are released; waited on before the first add
+        uint32_t* h = &S.htot[0][0];
+        for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
+        if (tid < 2 * kMaxCluster) (&S.cnt[0][0])[tid] = 0;
+        if (tid == 0) S.cand_n = 0;
+        __syncthreads();
+        cluster_arrive();  // zeroed totals are released; waited on before the first add
     }
 
     // ---- radix keys into shared memory: four float4 reads in flight -----
@@ -281,19 +261,83 @@ k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __rest
     __syncthreads();
     if (!single) cluster_wait();
 
-    // ---- digit rounds: bits 31..21, 20..10, 9..0 ----------------------------
+    // ---- digit rounds: bits 31..21, then 20..10 and 9..0 ----------------------
     uint32_t prefix = 0, mask = 0, kr = (uint32_t)k;
-    digit_round(keys_s, cnt, prefix, mask, 21, 2048, kr, single, 0, S);
+    digit_round(keys_s, cnt, prefix, mask, 21, 2048, kr, single, 0, CL, S);
     prefix |= S.pick[0] << 21;
     mask |= 0x7FFu << 21;
     kr -= S.pick[1];
-    digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, S);
-    prefix |= S.pick[0] << 10;
-    mask |= 0x7FFu << 10;
-    kr -= S.pick[1];
-    digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, S);
-    prefix |= S.pick[0];
-    kr -= S.pick[1];
+    const uint32_t in_bin = S.pick[2];  // keys of the row that share the first digit of T
+    if (!single && in_bin <= (uint32_t)kCandCap) {
+        // Few keys share the first digit: every slice sends those keys' values
+        // to CTA 0, which finds the exact k-th largest among them alone, then
+        // writes it (and the ties to take) into every slice.
+        uint32_t* cand = keys_s + ((slice_cap + 4 + 3) & ~3);
+        uint32_t mine = 0;
+        const int n4 = (cnt + 3) >> 2;
+        for (int i4 = tid; i4 < n4; i4 += kThreads) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys_s)[i4];
+            const int i = 4 * i4;
+            mine += (i + 0 < cnt && (u.x & mask) == prefix) + (i + 1 < cnt && (u.y & mask) == prefix) +
+                    (i + 2 < cnt && (u.z & mask) == prefix) + (i + 3 < cnt && (u.w & mask) == prefix);
+        }
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
+        }
+        if (lane == 31) S.wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t wv = S.wsum[lane];
+            uint32_t wi = wv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t x = __shfl_up_sync(kFull, wi, o);
+                if (lane >= o) wi += x;
+            }
+            S.wsum[lane] = wi - wv;
+            if (lane == 31 && wi) S.tot[0] = atom_add_remote(map_rank(&S.cand_n, 0), wi);  // reserve
+            if (lane == 31 && !wi) S.tot[0] = 0;
+        }
+        __syncthreads();
+        {
+            uint32_t at = S.tot[0] + S.wsum[warp] + incl - mine;
+            const uint32_t rc = map_rank(cand, 0);
+            for (int i4 = tid; i4 < n4; i4 += kThreads) {
+                const uint4 u = reinterpret_cast<const uint4*>(keys_s)[i4];
+                const int i = 4 * i4;
+                if (i + 0 < cnt && (u.x & mask) == prefix) st_remote(rc + 4 * at++, u.x);
+                if (i + 1 < cnt && (u.y & mask) == prefix) st_remote(rc + 4 * at++, u.y);
+                if (i + 2 < cnt && (u.z & mask) == prefix) st_remote(rc + 4 * at++, u.z);
+                if (i + 3 < cnt && (u.w & mask) == prefix) st_remote(rc + 4 * at++, u.w);
+            }
+        }
+        cluster_arrive();
+        cluster_wait();  // every candidate has landed in CTA 0
+        if (c == 0) {
+            const int nc = (int)S.cand_n;  // == in_bin
+            digit_round(cand, nc, prefix, mask, 10, 2048, kr, true, 1, CL, S);
+            uint32_t p2 = prefix | (S.pick[0] << 10), k2 = kr - S.pick[1];
+            digit_round(cand, nc, p2, mask | (0x7FFu << 10), 0, 1024, k2, true, 2, CL, S);
+            p2 |= S.pick[0];
+            k2 -= S.pick[1];
+            if (tid < 2 * CL) st_remote(map_rank(&S.bcast[tid & 1], (uint32_t)(tid >> 1)), (tid & 1) ? k2 : p2);
+        }
+        cluster_arrive();
+        cluster_wait();  // T and kr are in every slice
+        prefix = S.bcast[0];
+        kr = S.bcast[1];
+    } else {
+        digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, CL, S);
+        prefix |= S.pick[0] << 10;
+        mask |= 0x7FFu << 10;
+        kr -= S.pick[1];
+        digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, S);
+        prefix |= S.pick[0];
+        kr -= S.pick[1];
+    }
     const uint32_t T = prefix;            // the k-th largest radix key of the row
     const uint32_t gt_total = (uint32_t)k - kr;
 
@@ -338,18 +382,20 @@ k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __rest
     if (single) {
         if (tid < 2) S.base[tid] = 0;
     } else {
-        if (tid < 2) st_remote(map_rank(&S.cnt[tid][c], 0), S.tot[tid]);
+        // this slice's counts into every later slice
+        if (tid < 2 * kMaxCluster) {
+            const int a = tid / kMaxCluster, t = tid % kMaxCluster;
+            if ((uint32_t)t > c && t < CL) st_remote(map_rank(&S.cnt[a][c], (uint32_t)t), S.tot[a]);
+        }
         cluster_arrive();
-        cluster_wait();  // every slice's counts are in CTA 0
+        cluster_wait();  // every earlier slice's counts have landed; no remote access follows
         if (warp == 0) {  // lanes 0..15: counts above T, 16..31: counts at T
             const int a = lane >> 4, r = lane & 15;
-            uint32_t v = (uint32_t)r < c ? ld_remote(map_rank(&S.cnt[a][r], 0)) : 0u;
+            uint32_t v = (uint32_t)r < c ? S.cnt[a][r] : 0u;
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
             if (r == 0) S.base[a] = v;
         }
-        __syncthreads();
-        cluster_arrive();  // done reading CTA 0; waited on before leaving
     }
     __syncthreads();
 
@@ -391,7 +437,6 @@ k_select(const float* __restrict__ scores, int64_t stride, const int32_t* __rest
             }
         }
     }
-    if (!single) cluster_wait();  // CTA 0 outlives every remote read of its memory
 }
 
 int slice_cap_for(int cl, int64_t max_len) {
@@ -415,7 +460,7 @@ cudaError_t launch_c(const SelectArgs& a) {
             if (err != cudaSuccess) return err;
         }
         err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSliceCapMax * 4 + 16);
+                                   (kSliceCapMax + 8) * 4 + kCandCap * 4);
         if (err != cudaSuccess) return err;
         err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                    cudaSharedmemCarveoutMaxShared);
@@ -426,7 +471,7 @@ cudaError_t launch_c(const SelectArgs& a) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, (unsigned)a.R, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)cap * 4 + 16;
+    cfg.dynamicSmemBytes = (size_t)((cap + 4 + 3) & ~3) * 4 + (size_t)kCandCap * 4;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -435,7 +480,8 @@ cudaError_t launch_c(const SelectArgs& a) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_select<CL>, a.scores, a.score_stride, a.row_lens, a.k, a.indices,
+    const int64_t cap_len = a.len_cap < a.score_stride ? a.len_cap : a.score_stride;
+    return cudaLaunchKernelEx(&cfg, k_select<CL>, a.scores, cap_len, a.row_lens, a.score_stride, a.k, a.indices,
                               a.status, cap);
 }
 
@@ -445,7 +491,7 @@ bool cluster16_supported() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSliceCapMax * 4 + 16;
+        cfg.dynamicSmemBytes = (kSliceCapMax + 8) * 4 + kCandCap * 4;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 16;
@@ -457,7 +503,7 @@ bool cluster16_supported() {
         cudaError_t e = cudaFuncSetAttribute(k_select<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_select<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSliceCapMax * 4 + 16);
+                                     (kSliceCapMax + 8) * 4 + kCandCap * 4);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&nclusters, k_select<16>, &cfg);
         ok = (e == cudaSuccess && nclusters > 0) ? 1 : 0;
         (void)cudaGetLastError();  // a refused query leaves no sticky error

@@ -104,7 +104,7 @@ def test_config1_full():
     s, st = gpu_scores(w, sentinel=SENTINEL)
     assert st == 0
     worst = _assert_scores(w, s)
-    print("config 1 worst relative score error %.3g" % worst)
+    print("1 row x 4,096 keys: worst relative score error %.3g" % worst)
 
 
 def test_bad_block_id_is_reported():

@@ -54,11 +54,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 def test_noalloc_rejects_too_many_rows():
     lib = binding.load()
-    w = W.make_workload([[100] for _ in range(65)], "random", seed=73)
+    w = W.make_workload([[4] for _ in range(binding.MAX_ROWS + 1)], "random", seed=73)
     t = device_inputs(w)
     out = torch.zeros(w.R, 100, dtype=torch.float32, device="cuda")
     st = lib.idx_score_noalloc(0, t["q"].data_ptr(), t["head_w"].data_ptr(), t["k_cache"].data_ptr(),
                                t["k_scale"].data_ptr(), w.pool_pages, t["block_table"].data_ptr(),
                                w.max_pages, t["seq_lens"].data_ptr(), t["row_req"].data_ptr(), w.R,
                                out.data_ptr(), 100, torch.cuda.current_stream().cuda_stream)
-    assert st == -1  # IDX_ERR_ARG: more rows than the static scratch holds
+    assert st == -1  # IDX_ERR_ARG: more rows than the entry point takes
