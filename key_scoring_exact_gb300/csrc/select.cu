@@ -15,23 +15,20 @@
 //    folded into +0, NaN below every number).  The rounds run one compact
 //    loop body, so a one-shot launch does not refetch unrolled code.
 //  * Digits of 11, 11 and 10 bits: three rounds give the exact k-th largest
-//    image T and the number kr of keys equal to T that the list takes.
-//  * Histograms are built in shared memory with warp-aggregated atomics (the
-//    lanes sharing a hot digit add once); each slice then adds its non-zero
-//    bins into every slice's own totals with distributed-shared-memory
-//    reductions, so after one hardware cluster barrier each slice scans its
-//    local totals.  No slice spins on another; every wait is a cluster
-//    barrier.
-//  * After the first round, when the bin that holds the k-th key has at most
-//    8,192 keys across the row, every slice appends its keys of that bin to a
-//    candidate array in CTA 0 (a remote atomic reserves the room), and CTA 0
-//    alone runs the last two rounds on them, then writes T and kr into every
-//    slice: two rounds without a cluster barrier each.  A fuller bin takes
-//    the last two rounds on all slices as above.
-//  * Each slice then counts its keys above / at T and adds the counts to every
-//    later slice; after one more barrier the counts of earlier slices give its
-//    output offsets, and positions are written in order: keys above T first,
-//    then ties, each in ascending position.
+//    image T and the number kr of keys equal to T that the list takes.  The
+//    first round's histogram is built while the slice is loaded.
+//  * Histograms are built in shared memory with plain atomic adds (on this
+//    hardware faster than aggregating equal digits within a warp first, even
+//    when the scores crowd into a few bins); each slice then adds its
+//    non-zero bins into every slice's own totals with distributed-shared-
+//    memory reductions, so after one hardware cluster barrier each slice
+//    scans its local totals.  No slice spins on another; every wait is a
+//    cluster barrier.
+//  * Each thread then owns a contiguous run of the slice's positions: one
+//    block scan of its packed (above T, at T) counts gives its offsets within
+//    the slice, each slice adds its totals into every later slice, and after
+//    one more barrier the positions are written in order: keys above T
+//    first, then ties, each in ascending position.
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -39,13 +36,16 @@ namespace idx {
 
 namespace {
 
-constexpr int kThreads = 1024;
+#ifndef IDX_SELECT_THREADS
+#define IDX_SELECT_THREADS 1024
+#endif
+constexpr int kThreads = IDX_SELECT_THREADS;
 constexpr int kWarps = kThreads / 32;
+static_assert(kThreads >= 256 && kThreads <= 1024 && kThreads % 256 == 0, "block size");
+constexpr int kLoadUnroll = 4096 / kThreads;  // float4 reads in flight per thread (16K keys a CTA)
 constexpr int kBinsMax = 2048;
 constexpr int kSliceTarget = 4096;  // keys per slice the launcher aims for
 constexpr int kSliceCapMax = 32768; // keys one slice can hold (128 KB of shared memory)
-constexpr int kMaxChunks = kSliceCapMax / (4 * kThreads);
-constexpr int kCandCap = 8192;      // candidates CTA 0 resolves alone after the first round
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -74,10 +74,12 @@ __device__ __forceinline__ void red_add_remote(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void st_remote(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t atom_add_remote(uint32_t addr, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-    return old;
+__device__ __forceinline__ uint4 ld_remote4(uint32_t addr) {  // addr 16-byte aligned
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t radix_key(float x) {
@@ -87,75 +89,114 @@ __device__ __forceinline__ uint32_t radix_key(float x) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Add one key per lane (where `hit`) to histogram h: the lanes that share
-// the first hit lane's digit add together (the hot bin of a concentrated
-// score distribution), the rest alone.
-__device__ __forceinline__ void hist_add(uint32_t* h, bool hit, uint32_t d, int lane) {
-    const uint32_t m = __ballot_sync(kFull, hit);
-    if (m == 0) return;
-    const int leader = __ffs(m) - 1;
-    const uint32_t dl = __shfl_sync(kFull, d, leader);
-    const uint32_t same = __ballot_sync(kFull, hit && d == dl);
-    if (lane == leader) atomicAdd(&h[dl], (uint32_t)__popc(same));
-    if (hit && !((same >> lane) & 1u)) atomicAdd(&h[d], 1u);
-}
-
-struct Shared {
+struct __align__(16) Shared {
     uint32_t hloc[kBinsMax];             // this slice's histogram of the round
     uint32_t htot[3][kBinsMax];          // totals of every slice, one buffer per round
     uint32_t cnt[2][kMaxCluster];        // counts above / at T of every earlier slice
     uint32_t wsum[kWarps];
     uint32_t pick[3];                    // digit, keys above it, keys in it
-    uint32_t cand_n;                     // candidates gathered so far (CTA 0's copy)
-    uint32_t bcast[2];                   // T and kr, written by CTA 0 into every slice
-    uint32_t woff[2][kMaxChunks * kWarps];  // per (chunk, warp) counts, then offsets
-    uint32_t tot[2];                     // this slice's counts above / at T
-    uint32_t base[2];                    // counts of the earlier slices
 };
 
+// Exclusive prefix sum over the block in thread order; *total gets the sum.
+// Ends with a barrier, so S.wsum may be reused right after.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, Shared& S) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    const uint32_t wv = lane < kWarps ? S.wsum[lane] : 0u;
+    uint32_t wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(kFull, wi, o);
+        if (lane >= o) wi += x;
+    }
+    const uint32_t before = __shfl_sync(kFull, wi - wv, warp);
+    *total = __shfl_sync(kFull, wi, 31);
+    __syncthreads();
+    return before + incl - v;
+}
+
 // One digit round (digit = (key >> shift) & (nb - 1)) over the slice's keys
-// whose bits above the digit equal `prefix` under `mask`.  Leaves the digit
-// holding rank kr (counted from the largest digit) and the number of keys
-// above it in S.pick.  One copy of this code serves all rounds.
+// whose bits above the digit equal `prefix` under `mask` (or over S.hloc as
+// built by the caller, when `have_hist`).  Leaves the digit holding rank kr
+// (counted from the largest digit), the number of keys above it and the
+// number in it in S.pick.  One copy of this code serves all rounds.
 __device__ __noinline__ void digit_round(const uint32_t* __restrict__ keys, int cnt, uint32_t prefix,
                                          uint32_t mask, int shift, int nb, uint32_t kr, bool single, int r,
-                                         int nslices, Shared& S) {
+                                         int nslices, bool have_hist, Shared& S) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
-    __syncthreads();
-    const uint32_t dm = (uint32_t)nb - 1;
-    const int n4 = (cnt + 3) >> 2;
-    const int span = (n4 + 31) & ~31;  // whole warps take each trip
+    if (!have_hist) {
+        for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
+        __syncthreads();
+        const uint32_t dm = (uint32_t)nb - 1;
+        const int n4 = (cnt + 3) >> 2;
 #pragma unroll 1
-    for (int i4 = tid; i4 < span; i4 += kThreads) {
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (i4 < n4) u = reinterpret_cast<const uint4*>(keys)[i4];
-        const int i = 4 * i4;
-        hist_add(S.hloc, i + 0 < cnt && (u.x & mask) == prefix, (u.x >> shift) & dm, lane);
-        hist_add(S.hloc, i + 1 < cnt && (u.y & mask) == prefix, (u.y >> shift) & dm, lane);
-        hist_add(S.hloc, i + 2 < cnt && (u.z & mask) == prefix, (u.z >> shift) & dm, lane);
-        hist_add(S.hloc, i + 3 < cnt && (u.w & mask) == prefix, (u.w >> shift) & dm, lane);
+        for (int i4 = tid; i4 < n4; i4 += kThreads) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys)[i4];
+            const int i = 4 * i4;
+            if (i + 0 < cnt && (u.x & mask) == prefix) atomicAdd(&S.hloc[(u.x >> shift) & dm], 1u);
+            if (i + 1 < cnt && (u.y & mask) == prefix) atomicAdd(&S.hloc[(u.y >> shift) & dm], 1u);
+            if (i + 2 < cnt && (u.z & mask) == prefix) atomicAdd(&S.hloc[(u.z >> shift) & dm], 1u);
+            if (i + 3 < cnt && (u.w & mask) == prefix) atomicAdd(&S.hloc[(u.w >> shift) & dm], 1u);
+        }
     }
     __syncthreads();
-    const uint32_t* totals = S.hloc;
-    if (!single) {
-        // every non-zero bin into every slice's totals for this round
+    // Scan in descending digit order: thread tid < nb / bpt holds the bpt
+    // digits b0 .. b0 + bpt - 1 (tv[q] = digit b0 + q), b0 = nb - bpt (tid + 1),
+    // so threads in order cover the digits from the largest down; others none.
+    constexpr int kBptMax = kBinsMax / kThreads < 4 ? 4 : kBinsMax / kThreads;
+    const int bpt = nb / kThreads < 4 ? 4 : nb / kThreads;
+    const int b0 = nb - bpt * (tid + 1);
+    uint32_t tv[kBptMax];
+#pragma unroll
+    for (int q = 0; q < kBptMax; ++q) tv[q] = 0u;
+    if (single) {
+        if (b0 >= 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < kBptMax / 4; ++q4) {
+                if (4 * q4 < bpt) {
+                    const uint4 t4 = *reinterpret_cast<const uint4*>(&S.hloc[b0 + 4 * q4]);
+                    tv[4 * q4 + 0] = t4.x;
+                    tv[4 * q4 + 1] = t4.y;
+                    tv[4 * q4 + 2] = t4.z;
+                    tv[4 * q4 + 3] = t4.w;
+                }
+            }
+        }
+    } else {
+        // Bin b's total lives in slice b / (nb / nslices): each slice adds its
+        // non-zero bins there (one remote add per bin), and after the barrier
+        // every thread reads its bins' totals from their owner, four at a time.
+        const int per_owner = nb / nslices;
         for (int b = tid; b < nb; b += kThreads) {
             const uint32_t v = S.hloc[b];
-            if (v)
-                for (int t = 0; t < nslices; ++t) red_add_remote(map_rank(&S.htot[r][b], (uint32_t)t), v);
+            if (v) red_add_remote(map_rank(&S.htot[r][b], (uint32_t)(b / per_owner)), v);
         }
         cluster_arrive();
         cluster_wait();
-        totals = S.htot[r];
+        if (b0 >= 0) {
+            const uint32_t own = (uint32_t)(b0 / per_owner);
+#pragma unroll
+            for (int q4 = 0; q4 < kBptMax / 4; ++q4) {
+                if (4 * q4 < bpt) {
+                    const uint4 t4 = ld_remote4(map_rank(&S.htot[r][b0 + 4 * q4], own));
+                    tv[4 * q4 + 0] = t4.x;
+                    tv[4 * q4 + 1] = t4.y;
+                    tv[4 * q4 + 2] = t4.z;
+                    tv[4 * q4 + 3] = t4.w;
+                }
+            }
+        }
     }
-    // Scan in descending digit order: thread tid holds digits nb-1-(bpt*tid+q).
-    const int bpt = nb / kThreads;  // 2 or 1
-    uint32_t tv[2] = {0u, 0u}, sum = 0;
-    for (int q = 0; q < bpt; ++q) {
-        tv[q] = totals[nb - 1 - (bpt * tid + q)];
-        sum += tv[q];
-    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int q = 0; q < kBptMax; ++q) sum += tv[q];
     uint32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -165,24 +206,27 @@ __device__ __noinline__ void digit_round(const uint32_t* __restrict__ keys, int 
     if (lane == 31) S.wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {  // exclusive prefix of the warp totals
-        const uint32_t wv = S.wsum[lane];
+        const uint32_t wv = lane < kWarps ? S.wsum[lane] : 0u;
         uint32_t wi = wv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t x = __shfl_up_sync(kFull, wi, o);
             if (lane >= o) wi += x;
         }
-        S.wsum[lane] = wi - wv;
+        if (lane < kWarps) S.wsum[lane] = wi - wv;
     }
     __syncthreads();
     uint32_t above = S.wsum[warp] + incl - sum;
-    for (int q = 0; q < bpt; ++q) {
-        if (above < kr && above + tv[q] >= kr) {
-            S.pick[0] = (uint32_t)(nb - 1 - (bpt * tid + q));
-            S.pick[1] = above;
-            S.pick[2] = tv[q];
+#pragma unroll
+    for (int q = kBptMax - 1; q >= 0; --q) {
+        if (q < bpt) {
+            if (above < kr && above + tv[q] >= kr) {
+                S.pick[0] = (uint32_t)(b0 + q);
+                S.pick[1] = above;
+                S.pick[2] = tv[q];
+            }
+            above += tv[q];
         }
-        above += tv[q];
     }
     __syncthreads();
 }
@@ -191,11 +235,27 @@ template <int CL>
 __global__ void __launch_bounds__(kThreads)
 k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __restrict__ row_lens,
          int64_t stride, int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap) {
-    extern __shared__ __align__(16) uint32_t keys_s[];  // slice_cap radix keys
+    extern __shared__ __align__(16) uint32_t keys_s[];  // slice_cap radix keys (+ 4)
     __shared__ Shared S;
     const uint32_t c = cluster_ctarank();
     const int row = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
+
+    // Slice c covers positions [c * slice_cap, (c + 1) * slice_cap) of the row
+    // (slice_cap is fixed by the launch's length bound), so its score loads
+    // are issued together with the read of the row's length.
+    const int64_t start = (int64_t)c * slice_cap;
+    const float* src = scores + (int64_t)row * stride + start;
+    const int64_t lim64 = len_cap - start;  // keys of this slice inside the score buffer
+    const int lim = lim64 <= 0 ? 0 : (lim64 < slice_cap ? (int)lim64 : slice_cap);
+    const int lim4 = lim >> 2;
+    const float4* src4 = reinterpret_cast<const float4*>(src);
+    float4 v[kLoadUnroll];
+#pragma unroll
+    for (int u = 0; u < kLoadUnroll; ++u) {
+        const int i = u * kThreads + tid;
+        if (i < lim4) v[u] = __ldg(src4 + i);
+    }
 
     int64_t n = row_lens[row];
     if (n < 0 || n > len_cap) {
@@ -212,228 +272,123 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
             for (int j = tid; j < k; j += kThreads) dst[j] = j < n ? j : -1;
         return;
     }
-
-    // ---- slice plan ------------------------------------------------------
-    int64_t ns = (n + kSliceTarget - 1) / kSliceTarget;
-    if (ns > CL) ns = CL;
-    int64_t per = (n + ns - 1) / ns;
-    per = (per + 3) & ~int64_t(3);  // slice starts stay 16-byte aligned
-    if (per > slice_cap) per = slice_cap;
-    const bool single = ns == 1;
+    const bool single = n <= slice_cap;
     if (single && c != 0) return;   // one CTA serves the row; no cluster barrier is used
-    const int64_t start = (int64_t)c * per;
-    const int cnt = (int)(start < n ? (n - start < per ? n - start : per) : 0);
-    const float* src = scores + (int64_t)row * stride + start;
+    const int cnt = (int)(start < n ? (n - start < slice_cap ? n - start : slice_cap) : 0);
 
+    for (int i = tid; i < kBinsMax; i += kThreads) S.hloc[i] = 0;
     if (!single) {
         uint32_t* h = &S.htot[0][0];
         for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
         if (tid < 2 * kMaxCluster) (&S.cnt[0][0])[tid] = 0;
-        if (tid == 0) S.cand_n = 0;
-        __syncthreads();
-        cluster_arrive();  // zeroed totals are released; waited on before the first add
     }
+    __syncthreads();
+    if (!single) cluster_arrive();  // zeroed totals are released; waited on before the first add
 
-    // ---- radix keys into shared memory: four float4 reads in flight -----
+    // ---- radix keys into shared memory and the first round's histogram
+    //      (bits 31..21), 16K keys' reads in flight ---------------------------------
     {
         const int n4 = cnt >> 2;
-        const float4* src4 = reinterpret_cast<const float4*>(src);
         uint4* k4 = reinterpret_cast<uint4*>(keys_s);
 #pragma unroll 1
-        for (int b = 0; b < n4; b += 4 * kThreads) {
-            float4 v[4];
+        for (int b = 0; b < n4; b += kLoadUnroll * kThreads) {
+            if (b > 0) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = b + u * kThreads + tid;
-                if (i < n4) v[u] = __ldg(src4 + i);
+                for (int u = 0; u < kLoadUnroll; ++u) {
+                    const int i = b + u * kThreads + tid;
+                    if (i < n4) v[u] = __ldg(src4 + i);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kLoadUnroll; ++u) {
                 const int i = b + u * kThreads + tid;
-                if (i < n4)
-                    k4[i] = make_uint4(radix_key(v[u].x), radix_key(v[u].y), radix_key(v[u].z),
-                                       radix_key(v[u].w));
+                if (i < n4) {
+                    const uint4 key = make_uint4(radix_key(v[u].x), radix_key(v[u].y), radix_key(v[u].z),
+                                                 radix_key(v[u].w));
+                    k4[i] = key;
+                    atomicAdd(&S.hloc[key.x >> 21], 1u);
+                    atomicAdd(&S.hloc[key.y >> 21], 1u);
+                    atomicAdd(&S.hloc[key.z >> 21], 1u);
+                    atomicAdd(&S.hloc[key.w >> 21], 1u);
+                }
             }
         }
         const int tail = cnt & 3;
-        if (tid < 4) keys_s[4 * n4 + tid] = tid < tail ? radix_key(__ldg(src + 4 * n4 + tid)) : 0u;
+        if (tid < 4) {
+            const uint32_t key = tid < tail ? radix_key(__ldg(src + 4 * n4 + tid)) : 0u;
+            keys_s[4 * n4 + tid] = key;
+            if (tid < tail) atomicAdd(&S.hloc[key >> 21], 1u);
+        }
     }
     __syncthreads();
     if (!single) cluster_wait();
 
     // ---- digit rounds: bits 31..21, then 20..10 and 9..0 ----------------------
     uint32_t prefix = 0, mask = 0, kr = (uint32_t)k;
-    digit_round(keys_s, cnt, prefix, mask, 21, 2048, kr, single, 0, CL, S);
-    prefix |= S.pick[0] << 21;
-    mask |= 0x7FFu << 21;
-    kr -= S.pick[1];
-    const uint32_t in_bin = S.pick[2];  // keys of the row that share the first digit of T
-    if (!single && in_bin <= (uint32_t)kCandCap) {
-        // Few keys share the first digit: every slice sends those keys' values
-        // to CTA 0, which finds the exact k-th largest among them alone, then
-        // writes it (and the ties to take) into every slice.
-        uint32_t* cand = keys_s + ((slice_cap + 4 + 3) & ~3);
-        uint32_t mine = 0;
-        const int n4 = (cnt + 3) >> 2;
-        for (int i4 = tid; i4 < n4; i4 += kThreads) {
-            const uint4 u = reinterpret_cast<const uint4*>(keys_s)[i4];
-            const int i = 4 * i4;
-            mine += (i + 0 < cnt && (u.x & mask) == prefix) + (i + 1 < cnt && (u.y & mask) == prefix) +
-                    (i + 2 < cnt && (u.z & mask) == prefix) + (i + 3 < cnt && (u.w & mask) == prefix);
-        }
-        uint32_t incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += x;
-        }
-        if (lane == 31) S.wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const uint32_t wv = S.wsum[lane];
-            uint32_t wi = wv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t x = __shfl_up_sync(kFull, wi, o);
-                if (lane >= o) wi += x;
-            }
-            S.wsum[lane] = wi - wv;
-            if (lane == 31 && wi) S.tot[0] = atom_add_remote(map_rank(&S.cand_n, 0), wi);  // reserve
-            if (lane == 31 && !wi) S.tot[0] = 0;
-        }
-        __syncthreads();
-        {
-            uint32_t at = S.tot[0] + S.wsum[warp] + incl - mine;
-            const uint32_t rc = map_rank(cand, 0);
-            for (int i4 = tid; i4 < n4; i4 += kThreads) {
-                const uint4 u = reinterpret_cast<const uint4*>(keys_s)[i4];
-                const int i = 4 * i4;
-                if (i + 0 < cnt && (u.x & mask) == prefix) st_remote(rc + 4 * at++, u.x);
-                if (i + 1 < cnt && (u.y & mask) == prefix) st_remote(rc + 4 * at++, u.y);
-                if (i + 2 < cnt && (u.z & mask) == prefix) st_remote(rc + 4 * at++, u.z);
-                if (i + 3 < cnt && (u.w & mask) == prefix) st_remote(rc + 4 * at++, u.w);
-            }
-        }
-        cluster_arrive();
-        cluster_wait();  // every candidate has landed in CTA 0
-        if (c == 0) {
-            const int nc = (int)S.cand_n;  // == in_bin
-            digit_round(cand, nc, prefix, mask, 10, 2048, kr, true, 1, CL, S);
-            uint32_t p2 = prefix | (S.pick[0] << 10), k2 = kr - S.pick[1];
-            digit_round(cand, nc, p2, mask | (0x7FFu << 10), 0, 1024, k2, true, 2, CL, S);
-            p2 |= S.pick[0];
-            k2 -= S.pick[1];
-            if (tid < 2 * CL) st_remote(map_rank(&S.bcast[tid & 1], (uint32_t)(tid >> 1)), (tid & 1) ? k2 : p2);
-        }
-        cluster_arrive();
-        cluster_wait();  // T and kr are in every slice
-        prefix = S.bcast[0];
-        kr = S.bcast[1];
-    } else {
-        digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, CL, S);
-        prefix |= S.pick[0] << 10;
-        mask |= 0x7FFu << 10;
-        kr -= S.pick[1];
-        digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, S);
-        prefix |= S.pick[0];
+#pragma unroll 1
+    for (int r = 0; r < 3; ++r) {
+        const int shift = r == 0 ? 21 : (r == 1 ? 10 : 0);
+        const int nb = r == 2 ? 1024 : 2048;
+        digit_round(keys_s, cnt, prefix, mask, shift, nb, kr, single, r, CL, r == 0, S);
+        prefix |= S.pick[0] << shift;
+        mask |= (uint32_t)(nb - 1) << shift;
         kr -= S.pick[1];
     }
     const uint32_t T = prefix;            // the k-th largest radix key of the row
     const uint32_t gt_total = (uint32_t)k - kr;
 
-    // ---- counts per (chunk, warp), in position order.  Chunk j holds
-    //      positions [2048 j, 2048 j + 2048); thread tid covers 4 of them. ----
-    const int nchunks = (cnt + 4 * kThreads - 1) / (4 * kThreads);
-#pragma unroll 1
-    for (int j = 0; j < nchunks; ++j) {
-        const int i = 4 * (j * kThreads + tid);
-        const uint4 u = i < cnt ? reinterpret_cast<const uint4*>(keys_s)[j * kThreads + tid]
-                                : make_uint4(0, 0, 0, 0);
-        const uint32_t g = (i < cnt && u.x > T) + (i + 1 < cnt && u.y > T) + (i + 2 < cnt && u.z > T) +
-                           (i + 3 < cnt && u.w > T);
-        const uint32_t e = (i < cnt && u.x == T) + (i + 1 < cnt && u.y == T) + (i + 2 < cnt && u.z == T) +
-                           (i + 3 < cnt && u.w == T);
-        const uint32_t ga = __reduce_add_sync(kFull, g), ea = __reduce_add_sync(kFull, e);
-        if (lane == 0) {
-            S.woff[0][j * kWarps + warp] = ga;
-            S.woff[1][j * kWarps + warp] = ea;
-        }
+    // ---- thread tid owns the slice's positions [4 j0, 4 j1): its counts above
+    //      and at T, packed (above < 2^11, at <= slice_cap < 2^16), scanned in
+    //      thread order ------------------------------------------------------------
+    const int n4 = (cnt + 3) >> 2;
+    const int m4 = (n4 + kThreads - 1) / kThreads;
+    const int j0 = tid * m4 < n4 ? tid * m4 : n4;
+    const int j1 = j0 + m4 < n4 ? j0 + m4 : n4;
+    uint32_t mine = 0;
+    for (int j = j0; j < j1; ++j) {
+        const uint4 u = reinterpret_cast<const uint4*>(keys_s)[j];
+        const int i = 4 * j;
+        mine += ((uint32_t)(i + 0 < cnt && u.x > T) << 16) + (uint32_t)(i + 0 < cnt && u.x == T);
+        mine += ((uint32_t)(i + 1 < cnt && u.y > T) << 16) + (uint32_t)(i + 1 < cnt && u.y == T);
+        mine += ((uint32_t)(i + 2 < cnt && u.z > T) << 16) + (uint32_t)(i + 2 < cnt && u.z == T);
+        mine += ((uint32_t)(i + 3 < cnt && u.w > T) << 16) + (uint32_t)(i + 3 < cnt && u.w == T);
     }
-    __syncthreads();
-    if (warp == 0) {  // exclusive offsets over (chunk, warp) in position order
-        for (int a = 0; a < 2; ++a) {
-            uint32_t carry = 0;
-            for (int b0 = 0; b0 < nchunks * kWarps; b0 += 32) {
-                const int b = b0 + lane;
-                const uint32_t v = b < nchunks * kWarps ? S.woff[a][b] : 0u;
-                uint32_t inc = v;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t x = __shfl_up_sync(kFull, inc, o);
-                    if (lane >= o) inc += x;
-                }
-                if (b < nchunks * kWarps) S.woff[a][b] = carry + inc - v;
-                carry += __shfl_sync(kFull, inc, 31);
-            }
-            if (lane == 0) S.tot[a] = carry;
-        }
-    }
-    __syncthreads();
-    if (single) {
-        if (tid < 2) S.base[tid] = 0;
-    } else {
-        // this slice's counts into every later slice
-        if (tid < 2 * kMaxCluster) {
-            const int a = tid / kMaxCluster, t = tid % kMaxCluster;
-            if ((uint32_t)t > c && t < CL) st_remote(map_rank(&S.cnt[a][c], (uint32_t)t), S.tot[a]);
+    uint32_t total;
+    const uint32_t off = block_scan(mine, &total, S);
+    uint32_t base_gt = 0, base_eq = 0;
+    if (!single) {
+        // this slice's counts into every later slice (kept apart: a row's ties
+        // may outnumber 2^16)
+        if (tid > (int)c && tid < CL) {
+            st_remote(map_rank(&S.cnt[0][c], (uint32_t)tid), total >> 16);
+            st_remote(map_rank(&S.cnt[1][c], (uint32_t)tid), total & 0xFFFFu);
         }
         cluster_arrive();
         cluster_wait();  // every earlier slice's counts have landed; no remote access follows
-        if (warp == 0) {  // lanes 0..15: counts above T, 16..31: counts at T
-            const int a = lane >> 4, r = lane & 15;
-            uint32_t v = (uint32_t)r < c ? S.cnt[a][r] : 0u;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
-            if (r == 0) S.base[a] = v;
+        for (int t = 0; t < (int)c; ++t) {
+            base_gt += S.cnt[0][t];
+            base_eq += S.cnt[1][t];
         }
     }
-    __syncthreads();
 
     // ---- ordered writes --------------------------------------------------------
-#pragma unroll 1
-    for (int j = 0; j < nchunks; ++j) {
-        const int i = 4 * (j * kThreads + tid);
-        const uint4 u4 = i < cnt ? reinterpret_cast<const uint4*>(keys_s)[j * kThreads + tid]
-                                 : make_uint4(0, 0, 0, 0);
-        const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
-        uint32_t g = 0, e = 0;
+    if (mine) {
+        uint32_t pg = base_gt + (off >> 16);
+        uint32_t pe = gt_total + base_eq + (off & 0xFFFFu);
+        for (int j = j0; j < j1; ++j) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys_s)[j];
+            const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g += i + q < cnt && uu[q] > T;
-            e += i + q < cnt && uu[q] == T;
-        }
-        // exclusive prefix of the lanes before this one
-        uint32_t gi = g, ei = e;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t a = __shfl_up_sync(kFull, gi, o);
-            const uint32_t b = __shfl_up_sync(kFull, ei, o);
-            if (lane >= o) {
-                gi += a;
-                ei += b;
-            }
-        }
-        uint32_t pg = S.base[0] + S.woff[0][j * kWarps + warp] + gi - g;
-        uint32_t pe = gt_total + S.base[1] + S.woff[1][j * kWarps + warp] + ei - e;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (i + q >= cnt) break;
-            if (uu[q] > T) {
-                if (pg < gt_total) dst[pg] = (int32_t)(start + i + q);
-                ++pg;
-            } else if (uu[q] == T) {
-                if (pe < (uint32_t)k) dst[pe] = (int32_t)(start + i + q);
-                ++pe;
+            for (int q = 0; q < 4; ++q) {
+                const int i = 4 * j + q;
+                if (i >= cnt) break;
+                if (uu[q] > T) {
+                    if (pg < gt_total) dst[pg] = (int32_t)(start + i);
+                    ++pg;
+                } else if (uu[q] == T) {
+                    if (pe < (uint32_t)k) dst[pe] = (int32_t)(start + i);
+                    ++pe;
+                }
             }
         }
     }
@@ -448,30 +403,40 @@ int slice_cap_for(int cl, int64_t max_len) {
     return (int)(per < kSliceCapMax ? per : kSliceCapMax);
 }
 
+constexpr size_t slice_bytes(int cap) { return (size_t)((cap + 4 + 3) & ~3) * 4; }
+
+// Once per device: cluster and shared-memory attributes of k_select<CL>.
+template <int CL>
+cudaError_t configure(int dev) {
+    static int configured_device = -1;
+    if (configured_device == dev) return cudaSuccess;
+    cudaError_t err = cudaSuccess;
+    if (CL > 8) {
+        err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess) return err;
+    }
+    err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)slice_bytes(kSliceCapMax));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    configured_device = dev;
+    return cudaSuccess;
+}
+
 template <int CL>
 cudaError_t launch_c(const SelectArgs& a) {
-    static int configured_device = -1;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (configured_device != dev) {
-        if (CL > 8) {
-            err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (err != cudaSuccess) return err;
-        }
-        err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (kSliceCapMax + 8) * 4 + kCandCap * 4);
-        if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                   cudaSharedmemCarveoutMaxShared);
-        if (err != cudaSuccess) return err;
-        configured_device = dev;
-    }
+    err = configure<CL>(dev);
+    if (err != cudaSuccess) return err;
     const int cap = slice_cap_for(CL, a.max_len);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, (unsigned)a.R, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)((cap + 4 + 3) & ~3) * 4 + (size_t)kCandCap * 4;
+    cfg.dynamicSmemBytes = slice_bytes(cap);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -491,7 +456,7 @@ bool cluster16_supported() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = (kSliceCapMax + 8) * 4 + kCandCap * 4;
+        cfg.dynamicSmemBytes = 0;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 16;
@@ -499,11 +464,10 @@ bool cluster16_supported() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int nclusters = 0;
-        cudaError_t e = cudaFuncSetAttribute(k_select<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_select<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (kSliceCapMax + 8) * 4 + kCandCap * 4);
+        int nclusters = 0, dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = configure<16>(dev);
+        cfg.dynamicSmemBytes = slice_bytes(kSliceCapMax);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&nclusters, k_select<16>, &cfg);
         ok = (e == cudaSuccess && nclusters > 0) ? 1 : 0;
         (void)cudaGetLastError();  // a refused query leaves no sticky error

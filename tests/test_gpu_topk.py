@@ -61,6 +61,24 @@ def test_tie_heavy(levels):
     _check_rows(s, [n], 2048, got)
 
 
+def test_concentrated_values():
+    """Every score in one quarter-binade: the first 11-bit digit leaves all
+    keys in one bin, so the threshold is found in the next digits (the rows
+    take the selection's later gather points and, with heavy ties, its
+    general tail)."""
+    rng = np.random.default_rng(5)
+    n = 100000
+    lens = [n, n, n]
+    s = np.empty((3, n), np.float32)
+    s[0] = 1.0 + 0.25 * rng.random(n, dtype=np.float32) * np.float32(0.999)      # spread over 21 bits
+    s[1] = np.float32(1.0) + np.float32(2 ** -12) * rng.integers(0, 8, n)        # spread over the last 11 bits
+    s[2] = np.float32(3.0)                                                         # one value
+    s[2, 77777] = np.float32(3.5)
+    got, st = gpu_topk(s, lens, 2048)
+    assert st == 0
+    _check_rows(s, lens, 2048, got)
+
+
 def test_all_zero_row_is_iota():
     s = np.zeros((1, 10000), np.float32)
     got, st = gpu_topk(s, [10000], 2048)
