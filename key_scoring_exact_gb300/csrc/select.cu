@@ -127,7 +127,7 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, Shar
 // built by the caller, when `have_hist`).  Leaves the digit holding rank kr
 // (counted from the largest digit), the number of keys above it and the
 // number in it in S.pick.  One copy of this code serves all rounds.
-__device__ __noinline__ void digit_round(const uint32_t* __restrict__ keys, int cnt, uint32_t prefix,
+__device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, int cnt, uint32_t prefix,
                                          uint32_t mask, int shift, int nb, uint32_t kr, bool single, int r,
                                          int nslices, bool have_hist, Shared& S) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

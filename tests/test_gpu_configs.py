@@ -4,11 +4,13 @@ configuration on sampled positions), and every row's list bit-exact against
 the oracle's selection of the GPU's own scores."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
+from key_scoring_exact_gb300 import binding
 from key_scoring_exact_gb300 import workloads as W
 from tests import checks
-from tests.gpu_util import device_inputs, gpu_fused, problem
+from tests.gpu_util import device_inputs, gpu_fused, problem, stride_for
 
 pytestmark = pytest.mark.gpu
 
@@ -79,3 +81,19 @@ def test_fused_replay_determinism():
     for _ in range(10):
         s1, g1, _ = gpu_fused(w, t)
         assert np.array_equal(s0, s1) and np.array_equal(g0, g1)
+
+
+def test_fused_calls_share_one_workspace():
+    """One workspace across fused calls of different shapes: each call's
+    lists equal the oracle's lists of its own scores (nothing a call leaves
+    in the workspace changes the next one)."""
+    ws = binding.new_workspace(17, 131072, 2048)
+    for cfg in (2, 4, 1, 2, 3):
+        w = W.make_config(cfg)
+        t = device_inputs(w)
+        idx = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+        scores = torch.zeros(w.R, stride_for(w.max_len), dtype=torch.float32, device="cuda")
+        binding.score_topk(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"],
+                           t["seq_lens"], t["row_req"], w.max_len, w.k, idx, ws, scores=scores)
+        assert binding.check_status(ws) == 0
+        _lists_exact(w, scores.cpu().numpy(), idx.cpu().numpy())

@@ -79,6 +79,21 @@ def test_concentrated_values():
     _check_rows(s, lens, 2048, got)
 
 
+@pytest.mark.parametrize("n_tied", [1, 37, 300, 512, 513, 900])
+def test_ties_at_the_threshold(n_tied):
+    """A few hundred keys equal to the k-th score, spread over every slice of a
+    long row: the threshold's last digit and the ties are resolved on keys
+    gathered after two digits (up to 512 of them), or by the general tail."""
+    rng = np.random.default_rng(1000 + n_tied)
+    n = 120000
+    s = rng.standard_normal(n).astype(np.float32)
+    v = np.float32(np.sort(s)[::-1][2047 - n_tied // 2])  # near rank 2048
+    s[rng.choice(n, n_tied, replace=False)] = v
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
+
+
 def test_all_zero_row_is_iota():
     s = np.zeros((1, 10000), np.float32)
     got, st = gpu_topk(s, [10000], 2048)
