@@ -292,37 +292,36 @@ def copies_for(w, minimum: int) -> int:
 
 
 def e2e_time(st: Step, steps: int, stream):
-    """Through the public API with host buffers: per step, pinned H2D of the
-    step's inputs (query, head weights, block table, row lengths, row map),
-    idx_score_topk, D2H of the indices.  The key cache is device-resident
-    state (the serving KV cache), not a per-step input."""
+    """Through the public C ABI with host buffers: each step is one
+    idx_score_topk_host call, which copies that step's inputs (query, head
+    weights, block table, row lengths, row map) from pinned host memory,
+    runs the scoring and the selection, and copies the indices back to pinned
+    host memory.  The key cache is device-resident state (the serving KV
+    cache), not a per-step input.  Steps are issued back to back on one
+    stream; the timed region ends once the last step's indices are on the
+    host."""
     w = st.w
-    host_in = {"q": w.q.pin_memory(), "head_w": w.head_w.pin_memory(),
-               "tables": [t.cpu().pin_memory() for t in st.tables],
-               "seq_lens": w.seq_lens.pin_memory(), "row_req": w.row_req.pin_memory()}
+    host_q, host_w = w.q.contiguous().pin_memory(), w.head_w.contiguous().pin_memory()
+    host_tables = [t.cpu().contiguous().pin_memory() for t in st.tables]
+    host_lens, host_req = w.seq_lens.contiguous().pin_memory(), w.row_req.contiguous().pin_memory()
     out_host = torch.empty(st.R, st.k, dtype=torch.int32).pin_memory()
-    dq, dw = torch.empty_like(st.q), torch.empty_like(st.head_w)
-    dl, dr = torch.empty_like(st.seq_lens), torch.empty_like(st.row_req)
-    dt = torch.empty_like(st.tables[0])
-    h2d = (host_in["q"].numel() * host_in["q"].element_size() + host_in["head_w"].numel() * 4
-           + host_in["tables"][0].numel() * 4 + 2 * st.R * 4)
-    d2h = st.R * st.k * 4
     b = st.binding
+    n_req, max_pages = host_tables[0].shape
+    ws = b.new_host_workspace(st.R, st.max_len, st.k, n_req, max_pages)
+    h2d = (host_q.numel() * host_q.element_size() + host_w.numel() * 4 + host_tables[0].numel() * 4
+           + 2 * st.R * 4)
+    d2h = st.R * st.k * 4
 
     def one(i):
-        dq.copy_(host_in["q"], non_blocking=True)
-        dw.copy_(host_in["head_w"], non_blocking=True)
-        dt.copy_(host_in["tables"][i % st.copies], non_blocking=True)
-        dl.copy_(host_in["seq_lens"], non_blocking=True)
-        dr.copy_(host_in["row_req"], non_blocking=True)
-        b.score_topk(dq, dw, st.k_cache, st.k_scale, dt, dl, dr, st.max_len, st.k, st.idx, st.ws,
-                     scores=st.scores, stream=stream)
-        out_host.copy_(st.idx, non_blocking=True)
+        b.score_topk_host(host_q, host_w, st.k_cache, st.k_scale, host_tables[i % st.copies], host_lens,
+                          host_req, st.max_len, st.k, out_host, ws, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(3):
             one(i)
         torch.cuda.synchronize()
+        if b.check_status(ws, stream) != 0:
+            raise RuntimeError("device status in the end-to-end warm-up")
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(steps):

@@ -146,6 +146,42 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_host_workspace_bytes -- workspace bytes idx_score_topk_host needs for R
+ * rows of at most max_len keys, k, and a block table of n_req x max_pages.
+ * Returns 0 for arguments out of range.
+ */
+size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int max_pages);
+
+/*
+ * idx_score_topk_host -- the fused call (idx_score_topk) with the per-step
+ * inputs and the output in HOST memory: the key cache and its scales stay in
+ * device memory (the serving cache), while the query, head weights, block
+ * table (n_req x max_pages), row lengths, row map and the [R][k] indices are
+ * host buffers.  The call brings the inputs into the workspace, runs the
+ * scoring and the selection on `stream` (the scores live in the workspace),
+ * and returns the indices to indices_host.  Page-locked buffers that the
+ * driver maps into the device's address space (16-byte aligned inputs) are
+ * read by one gather kernel and the indices written by the selection kernel
+ * directly, over the CPU-GPU link; other host buffers go through
+ * cudaMemcpyAsync.  Everything is asynchronous: the indices are in
+ * indices_host once the stream has reached the end of the call (synchronise
+ * it, or wait on an event recorded after the call), and the host must not
+ * modify the inputs before then.
+ *
+ *  workspace  device memory, 1024-byte aligned, >= idx_host_workspace_bytes
+ *             (R, max_len, k, n_req, max_pages), zeroed once by idx_workspace_init
+ *
+ * Errors: those of idx_score_topk; IDX_ERR_ARG for a null host pointer or a
+ * size out of range, IDX_ERR_CUDA when a copy cannot be queued.
+ */
+idx_status idx_score_topk_host(int qtype, const void *q_host, const float *head_w_host,
+                               const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                               const int32_t *block_table_host, int n_req, int max_pages,
+                               const int32_t *seq_lens_host, const int32_t *row_req_host, int R,
+                               int64_t max_len, int k, int32_t *indices_host,
+                               void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_score_noalloc -- idx_score for callers that cannot allocate device
  * memory, with no workspace argument.  The paper has no counterpart to this
  * entry point; it exists for callers such as a serving loop replaying a

@@ -21,7 +21,8 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
           -4: "IDX_ERR_CUDA", -5: "IDX_ERR_TIMEOUT", -6: "IDX_ERR_BOUNDS", -7: "IDX_ERR_UNSUPPORTED"}
 
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
-           "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc")
+           "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
+           "idx_host_workspace_bytes", "idx_score_topk_host")
 
 _lib = None
 
@@ -67,6 +68,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_version.argtypes = []
     lib.idx_score_noalloc.restype = i32
     lib.idx_score_noalloc.argtypes = score_common + [p, i64, p]
+    lib.idx_host_workspace_bytes.restype = sz
+    lib.idx_host_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
+    lib.idx_score_topk_host.restype = i32
+    lib.idx_score_topk_host.argtypes = [i32, p, p, p, p, i64, p, i32, i32, p, p, i32, i64, i32, p, p, sz, p]
     _lib = lib
     return lib
 
@@ -182,6 +187,56 @@ def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_
                                stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(),
                                _stream(stream))
     _check(st, "idx_score_topk")
+
+
+def host_workspace_bytes(R: int, max_len: int, k: int, n_req: int, max_pages: int) -> int:
+    return int(load().idx_host_workspace_bytes(int(R), int(max_len), int(k), int(n_req), int(max_pages)))
+
+
+def new_host_workspace(R: int, max_len: int, k: int, n_req: int, max_pages: int, device=None,
+                       stream=None) -> torch.Tensor:
+    """A zero-initialised, 1024-byte aligned workspace for score_topk_host."""
+    n = host_workspace_bytes(R, max_len, k, n_req, max_pages)
+    if n == 0:
+        raise ValueError("invalid workspace request")
+    raw = torch.zeros(n + 1024, dtype=torch.uint8, device=device or "cuda")
+    off = (-raw.data_ptr()) % 1024
+    ws = raw[off:off + n]
+    _check(load().idx_workspace_init(ws.data_ptr(), n, _stream(stream)), "idx_workspace_init")
+    return ws
+
+
+def _host(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError("%s has dtype %s" % (name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def score_topk_host(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
+                    workspace, stream=None):
+    """idx_score_topk_host: q, head_w, block_table, seq_lens, row_req and the
+    [R, k] indices are host tensors (pin them for asynchronous copies); the
+    key cache, its scales and the workspace are device tensors.  Asynchronous:
+    read `indices` after synchronising the stream."""
+    R = q.shape[0]
+    if tuple(q.shape) != (R, HEADS, DIM) or tuple(head_w.shape) != (R, HEADS):
+        raise ValueError("q must be [R, 64, 128] and head_w [R, 64]")
+    if k_cache.dim() != 3 or tuple(k_cache.shape[1:]) != (PAGE, DIM) or tuple(k_scale.shape) != tuple(k_cache.shape[:2]):
+        raise ValueError("k_cache must be [pool_pages, 64, 128] and k_scale [pool_pages, 64]")
+    if block_table.dim() != 2 or seq_lens.shape != (R,) or row_req.shape != (R,) or indices.shape != (R, k):
+        raise ValueError("block_table [n_req, max_pages], seq_lens/row_req [R], indices [R, k]")
+    st = load().idx_score_topk_host(
+        _qtype(q), _host(q, "q"), _host(head_w, "head_w", torch.float32),
+        _dev(k_cache, "k_cache", (torch.uint8, torch.float8_e4m3fn)), _dev(k_scale, "k_scale", torch.float32),
+        int(k_cache.shape[0]), _host(block_table, "block_table", torch.int32), int(block_table.shape[0]),
+        int(block_table.shape[1]), _host(seq_lens, "seq_lens", torch.int32), _host(row_req, "row_req", torch.int32),
+        int(R), int(max_len), int(k), _host(indices, "indices", torch.int32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "idx_score_topk_host")
 
 
 def check_status(workspace, stream=None) -> int:

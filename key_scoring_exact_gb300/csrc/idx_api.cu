@@ -143,6 +143,42 @@ idx_status noalloc_scratch(char** out) {
 
 using namespace idx;
 
+namespace {
+// Host-buffer fused call: the fused call's workspace (scores inside), then
+// device copies of the per-step inputs and of the output indices.
+struct HostLayout {
+    size_t q, w, bt, lens, rreq, idx, end;
+};
+HostLayout host_layout(int R, int64_t max_len, int k, int n_req, int max_pages) {
+    HostLayout H{};
+    size_t at = ws_layout(R, max_len, 1).end;
+    auto take = [&at](size_t bytes) {
+        const size_t p = at;
+        at = align_up(at + bytes, 256);
+        return p;
+    };
+    H.q = take((size_t)R * kHeads * kDim * 2);
+    H.w = take((size_t)R * kHeads * 4);
+    H.bt = take((size_t)n_req * (size_t)max_pages * 4);
+    H.lens = take((size_t)R * 4);
+    H.rreq = take((size_t)R * 4);
+    H.idx = take((size_t)R * (size_t)k * 4);
+    H.end = align_up(at, 1024);
+    return H;
+}
+
+// The device address of a host buffer the GPU can reach (page-locked and
+// mapped into the device's address space), or null (pageable memory).
+const void* mapped(const void* host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+}  // namespace
+
 extern "C" {
 
 size_t idx_workspace_bytes(int R, int64_t max_len, int k, int with_scores) {
@@ -230,6 +266,72 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
     SelectArgs sel{scores, score_stride, seq_lens, R, k, indices,
                    reinterpret_cast<uint32_t*>(ws + L.status), max_len, max_len, s};
     return to_status(launch_select(sel));
+}
+
+size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int max_pages) {
+    if (R < 1 || R > kMaxRows || max_len < 1 || k < 1 || k > IDX_MAX_K || n_req < 1 || max_pages < 1) return 0;
+    return host_layout(R, max_len, k, n_req, max_pages).end;
+}
+
+idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_w_host, const uint8_t* k_cache,
+                               const float* k_scale, int64_t pool_pages, const int32_t* block_table_host,
+                               int n_req, int max_pages, const int32_t* seq_lens_host,
+                               const int32_t* row_req_host, int R, int64_t max_len, int k,
+                               int32_t* indices_host, void* workspace, size_t ws_bytes, void* stream) {
+    if (!q_host || !head_w_host || !block_table_host || !seq_lens_host || !row_req_host || !indices_host)
+        return IDX_ERR_ARG;
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (R < 1 || R > kMaxRows || n_req < 1 || max_pages < 1 || k < 1 || k > IDX_MAX_K || max_len < 1)
+        return IDX_ERR_ARG;
+    if (!workspace) return IDX_ERR_WORKSPACE;
+    if (!aligned(workspace, 1024)) return IDX_ERR_ALIGN;
+    const HostLayout H = host_layout(R, max_len, k, n_req, max_pages);
+    if (ws_bytes < H.end) return IDX_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Inputs in page-locked, mapped host memory are gathered by one kernel that
+    // reads them over the host link; any other buffer is copied by the copy engine.
+    const struct {
+        const void* host;
+        size_t off, bytes;
+    } in[kStageMaxCopies] = {
+        {q_host, H.q, (size_t)R * kHeads * kDim * (qtype == IDX_Q_BF16 ? 2 : 1)},
+        {head_w_host, H.w, (size_t)R * kHeads * 4},
+        {block_table_host, H.bt, (size_t)n_req * (size_t)max_pages * 4},
+        {seq_lens_host, H.lens, (size_t)R * 4},
+        {row_req_host, H.rreq, (size_t)R * 4},
+    };
+    StagePlan plan{};
+    for (const auto& b : in) {
+        const void* d = mapped(b.host);
+        if (d && aligned(d, 16) && b.bytes % 4 == 0 && b.bytes < (1ull << 31)) {
+            plan.c[plan.n++] = StageCopy{d, ws + b.off, (uint32_t)b.bytes};
+        } else if (cudaMemcpyAsync(ws + b.off, b.host, b.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return IDX_ERR_CUDA;
+        }
+    }
+    if (plan.n > 0 && launch_stage(plan, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    // The selection writes the indices straight into mapped host memory.
+    int32_t* idx_dev = reinterpret_cast<int32_t*>(ws + H.idx);
+    int32_t* idx_out = idx_dev;
+    const void* out_map = mapped(indices_host);
+    if (out_map && aligned(out_map, 4)) idx_out = const_cast<int32_t*>(static_cast<const int32_t*>(out_map));
+    const idx_status st = idx_score_topk(qtype, ws + H.q, reinterpret_cast<const float*>(ws + H.w), k_cache, k_scale,
+                                         pool_pages, reinterpret_cast<const int32_t*>(ws + H.bt), max_pages,
+                                         reinterpret_cast<const int32_t*>(ws + H.lens),
+                                         reinterpret_cast<const int32_t*>(ws + H.rreq), R, max_len, k, idx_out,
+                                         nullptr, 0, workspace, ws_bytes, stream);
+    if (st != IDX_OK) return st;
+    if (idx_out == idx_dev &&
+        cudaMemcpyAsync(indices_host, idx_dev, (size_t)R * (size_t)k * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    return IDX_OK;
 }
 
 idx_status idx_check_status(void* workspace, void* stream) {

@@ -83,6 +83,20 @@ struct SelectArgs {
 };
 
 cudaError_t launch_select(const SelectArgs& a);
+
+// Device copies of host buffers the GPU can address (page-locked, mapped):
+// every source and destination 16-byte aligned, every size a multiple of 4.
+constexpr int kStageMaxCopies = 5;
+struct StageCopy {
+    const void* src;
+    void* dst;
+    uint32_t bytes;
+};
+struct StagePlan {
+    StageCopy c[kStageMaxCopies];
+    int n;
+};
+cudaError_t launch_stage(const StagePlan& plan, cudaStream_t stream);
 // Longest row the selection handles with clusters of `cluster` CTAs.
 int64_t select_max_len(int cluster);
 constexpr int64_t kSelectMaxLen = 16 * 512 * 4 * 16;  // 524,288 keys (16-CTA clusters)

@@ -58,3 +58,43 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.idx_topk(fake, 16, fake, 1, 0, fake, None, 0, None) == -1      # k = 0
     assert lib.idx_topk(fake, 16, fake, 1, 4096, fake, None, 0, None) == -1   # k > 2048
     assert lib.idx_topk(fake, 18, fake, 1, 8, fake, None, 0, None) == -2      # stride % 4
+
+
+def test_host_entry_sizes_and_argument_errors(lib):
+    """The host-buffer fused call: its workspace holds the fused call's
+    workspace (scores inside) plus device copies of the inputs and indices;
+    null host pointers and sizes out of range are refused before any copy."""
+    lib.idx_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.idx_host_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int]
+    lib.idx_workspace_bytes.restype = ctypes.c_size_t
+    lib.idx_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    h = lib.idx_host_workspace_bytes(4, 131072, 2048, 1, 2048)
+    fused = lib.idx_workspace_bytes(4, 131072, 2048, 1)
+    inputs = 4 * 64 * 128 * 2 + 4 * 64 * 4 + 2048 * 4 + 2 * 4 * 4 + 4 * 2048 * 4
+    assert h >= fused + inputs and h % 1024 == 0
+    assert lib.idx_host_workspace_bytes(0, 100, 2048, 1, 2) == 0
+    assert lib.idx_host_workspace_bytes(4, 100, 4096, 1, 2) == 0
+    assert lib.idx_host_workspace_bytes(4, 100, 2048, 0, 2) == 0
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.idx_score_topk_host.restype = ctypes.c_int
+    lib.idx_score_topk_host.argtypes = [i32, p, p, p, p, i64, p, i32, i32, p, p, i32, i64, i32, p, p, sz, p]
+    buf = (ctypes.c_char * 4096)()
+    hp = ctypes.cast(buf, p)
+    fake = ctypes.c_void_p(1024)
+    args = [0, hp, hp, fake, fake, 8, hp, 1, 4, hp, hp, 1, 256, 16, hp, fake, 1 << 30, None]
+    bad_q = list(args)
+    bad_q[1] = None
+    assert lib.idx_score_topk_host(*bad_q) == -1                 # null host query
+    bad_k = list(args)
+    bad_k[13] = 0
+    assert lib.idx_score_topk_host(*bad_k) == -1                 # k = 0
+    bad_t = list(args)
+    bad_t[0] = 7
+    assert lib.idx_score_topk_host(*bad_t) == -1                 # query type
+    small = list(args)
+    small[16] = 1024
+    assert lib.idx_score_topk_host(*small) == -3                 # workspace too small
+    odd = list(args)
+    odd[15] = ctypes.c_void_p(1024 + 256)
+    assert lib.idx_score_topk_host(*odd) == -2                   # workspace alignment

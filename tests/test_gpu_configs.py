@@ -97,3 +97,21 @@ def test_fused_calls_share_one_workspace():
                            t["seq_lens"], t["row_req"], w.max_len, w.k, idx, ws, scores=scores)
         assert binding.check_status(ws) == 0
         _lists_exact(w, scores.cpu().numpy(), idx.cpu().numpy())
+
+
+@pytest.mark.parametrize("cfg,pinned", [(2, True), (4, True), (1, False)])
+def test_host_buffer_call_matches_device_call(cfg, pinned):
+    """idx_score_topk_host (inputs and indices in host memory, page-locked or
+    not) gives the device call's lists."""
+    w = W.make_config(cfg)
+    t = device_inputs(w)
+    _, ref, st = gpu_fused(w, t)
+    assert st == 0
+    host = lambda x: x.contiguous().pin_memory() if pinned else x.contiguous()
+    ws = binding.new_host_workspace(w.R, w.max_len, w.k, w.block_table.shape[0], w.block_table.shape[1])
+    out = host(torch.full((w.R, w.k), -7, dtype=torch.int32))
+    binding.score_topk_host(host(w.q), host(w.head_w), t["k_cache"], t["k_scale"], host(w.block_table),
+                            host(w.seq_lens), host(w.row_req), w.max_len, w.k, out, ws)
+    torch.cuda.synchronize()
+    assert binding.check_status(ws) == 0
+    assert np.array_equal(out.numpy(), ref)
