@@ -64,6 +64,10 @@ def _load():
             lib.oracle_topk.argtypes = [p, i64, i32, p]
             lib.oracle_topk_rows.restype = i32
             lib.oracle_topk_rows.argtypes = [p, i64, p, i32, i32, p]
+            lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_quantize_query.restype = None
+            lib.oracle_quantize_query.argtypes = [p, p, i32, i32, i32, p, p]
             _lib = lib
     return _lib
 
@@ -96,6 +100,31 @@ def bf16_to_f64(bits) -> np.ndarray:
     for i, v in enumerate(c.reshape(-1).tolist()):
         flat[i] = lib.oracle_bf16_to_f64(v)
     return out
+
+
+def f32_to_e4m3(values) -> np.ndarray:
+    """Encode f32 values (any shape) as E4M3 codes, one by one: nearest,
+    ties to even, saturated at +-448, NaN to the NaN code."""
+    lib = _load()
+    c = _c(values, np.float32)
+    out = np.empty(c.shape, np.uint8)
+    flat = out.reshape(-1)
+    for i, v in enumerate(c.reshape(-1).tolist()):
+        flat[i] = lib.oracle_f32_to_e4m3(v)
+    return out
+
+
+def quantize_query(q_bits, head_w):
+    """FP8 query of a bf16 index query, one scale per (row, head):
+    returns (codes [R, H, D] uint8, w' [R, H] float32)."""
+    lib = _load()
+    q = _c(q_bits, np.uint16)
+    w = _c(head_w, np.float32)
+    R, H, D = q.shape
+    q8 = np.empty(q.shape, np.uint8)
+    wo = np.empty((R, H), np.float32)
+    lib.oracle_quantize_query(_ptr(q), _ptr(w), R, H, D, _ptr(q8), _ptr(wo))
+    return q8, wo
 
 
 class Problem:

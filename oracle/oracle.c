@@ -49,6 +49,31 @@ double oracle_e4m3_to_f64(uint8_t code)
     return sign ? -v : v;
 }
 
+/* Nearest E4M3 code of an f32 value, ties to the even mantissa, magnitudes
+ * beyond the largest finite value (448) saturated to +-448, NaN to the NaN
+ * code.  Written from the format definition: the magnitude is compared with
+ * every finite non-negative code (0x00 .. 0x7E, increasing with the code), and
+ * of two equally near codes the one with an even mantissa (even code) wins. */
+uint8_t oracle_f32_to_e4m3(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x))
+        return 0x7F;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(oracle_e4m3_to_f64((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
 /* bf16 is the upper half of an IEEE-754 binary32. */
 double oracle_bf16_to_f64(uint16_t bits)
 {
@@ -282,4 +307,38 @@ int oracle_topk_rows(const float *scores, int64_t stride, const int32_t *lens, i
             return st;
     }
     return OR_OK;
+}
+
+/* ------------------------------------------------ FP8 query quantisation */
+
+/* The FP8 (E4M3) query of a bf16 index query, one scale per (row, head):
+ * amax = the largest |q| of the head's elements, scale = amax / 448 in f32,
+ * code = E4M3(q / scale) (f32 division, nearest-even rounding, saturated),
+ * and the head weight w * scale in f32, so that w' * relu(code . k) equals
+ * w * relu((code * scale) . k).  A head whose elements are all zero gets
+ * scale 0: codes 0 and weight 0.  This is the per-token FP8 quantisation
+ * "amax / 448, clamp, round to nearest even" that "[Perf] [MI355X] minimax_m31"
+ * (section "Modifications", o_proj bullet) describes, applied per head to the
+ * index query; the division is taken as one correctly rounded f32 division.
+ * q and q8 are [R][H][D], head_w and w_out [R][H]. */
+void oracle_quantize_query(const uint16_t *q, const float *head_w, int R, int H, int D,
+                           uint8_t *q8, float *w_out)
+{
+    for (int r = 0; r < R; ++r)
+        for (int h = 0; h < H; ++h) {
+            const uint16_t *row = q + ((size_t)r * H + h) * D;
+            uint8_t *out = q8 + ((size_t)r * H + h) * D;
+            float amax = 0.0f;
+            for (int d = 0; d < D; ++d) {
+                const float a = fabsf((float)oracle_bf16_to_f64(row[d]));
+                if (a > amax)
+                    amax = a;
+            }
+            const float scale = amax / 448.0f;
+            w_out[(size_t)r * H + h] = head_w[(size_t)r * H + h] * scale;
+            for (int d = 0; d < D; ++d) {
+                const float x = (float)oracle_bf16_to_f64(row[d]);
+                out[d] = scale > 0.0f ? oracle_f32_to_e4m3(x / scale) : 0;
+            }
+        }
 }

@@ -360,3 +360,127 @@ def test_oracle_planted_mistake_is_caught():
     keys = kv[pb.block_table[0]].reshape(-1, pb.D)[:23]
     no_relu = np.einsum("h,hj->j", pb.head_w[0].astype(np.float64), np.einsum("hd,jd->hj", q[0], keys))
     assert np.max(np.abs(no_relu - ref[0])) > 1e-3
+
+
+# ---------------------------------------------------------------- FP8 query quantisation
+
+def _torch_e4m3_codes(x32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_midpoints() -> np.ndarray:
+    """Every value halfway between two neighbouring finite non-negative E4M3
+    values (an exact tie), with both signs."""
+    vals = oracle.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8)).reshape(-1)
+    mids = (vals[:-1] + vals[1:]) / 2
+    return np.concatenate([mids, -mids]).astype(np.float32)
+
+
+def test_e4m3_encode_matches_torch_cast():
+    """The oracle's encoder (nearest by exhaustive comparison, ties to even)
+    against torch's cast on every finite bf16 value below the saturation
+    point (|x| < 464, where the cast does not overflow), every exact tie and
+    its neighbours, and random f32 values."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) < 464)]
+    mids = _e4m3_midpoints()
+    near = np.concatenate([np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(-np.inf))])
+    rng = np.random.default_rng(9)
+    rnd = (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 8, 20000))).astype(np.float32)
+    rnd = rnd[np.abs(rnd) < 464]
+    x = np.concatenate([vals, mids, near, rnd]).astype(np.float32)
+    assert np.array_equal(oracle.f32_to_e4m3(x), _torch_e4m3_codes(x))
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    x = np.array([448.0, 463.9, 464.0, 500.0, 1e30, -464.0, -1e30, np.nan], np.float32)
+    assert oracle.f32_to_e4m3(x).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_exact_powers_of_two():
+    """Heads made of E4M3 values times 2^k with one element at 448 * 2^k: the
+    scale is exactly 2^k, so the codes are the E4M3 values and w' = w 2^k."""
+    rng = np.random.default_rng(31)
+    R, H, D = 2, 5, 128
+    codes = rng.integers(0, 0x7F, (R, H, D)).astype(np.uint8)
+    codes[rng.random((R, H, D)) < 0.5] |= 0x80
+    codes[codes == 0x80] = 0x00
+    codes[codes == 0xFF] = 0x7E
+    codes[..., 7] = 0x7E                         # the head's largest magnitude: 448
+    codes[..., 0x7F & 9] &= 0x7F                 # keep one position non-negative
+    vals = oracle.e4m3_to_f64(codes).astype(np.float32)
+    ks = rng.integers(-20, 20, (R, H)).astype(np.float32)
+    q = vals * np.exp2(ks)[:, :, None]
+    w = rng.uniform(0.1, 2.0, (R, H)).astype(np.float32)
+    q8, wo = oracle.quantize_query(_bf16_bits(q), w)
+    assert np.array_equal(q8, codes)
+    assert np.array_equal(wo, (w * np.exp2(ks)).astype(np.float32))
+
+
+def test_quantize_zero_and_single_element_heads():
+    R, H, D = 1, 3, 128
+    q = np.zeros((R, H, D), np.float32)
+    q[0, 1, 17] = -3.0
+    q[0, 2, 5] = 0.013671875
+    w = np.array([[1.5, 2.0, -0.5]], np.float32)
+    q8, wo = oracle.quantize_query(_bf16_bits(q), w)
+    assert not q8[0, 0].any() and wo[0, 0] == 0.0                     # an all-zero head
+    assert q8[0, 1, 17] == 0xFE and np.count_nonzero(q8[0, 1]) == 1   # -448
+    assert q8[0, 2, 5] == 0x7E and np.count_nonzero(q8[0, 2]) == 1
+    assert wo[0, 1] == np.float32(2.0) * (np.float32(3.0) / np.float32(448.0))
+    assert wo[0, 2] == np.float32(-0.5) * (np.float32(0.013671875) / np.float32(448.0))
+
+
+def _quant_properties_hold(q32, w, q8, wo) -> bool:
+    """Properties of any correct per-head amax/448 quantisation: the largest
+    element maps to +-448, w' / w is the head's scale, and every element is
+    reproduced within half an E4M3 step at its magnitude (times the scale),
+    give or take the f32 rounding of the quotient (2^-24 relative, well
+    below the 1e-5 of the half step allowed here)."""
+    amax = np.abs(q32).max(-1)
+    scale = (wo / w).astype(np.float64)
+    if not np.allclose(scale, amax.astype(np.float64) / 448, rtol=1e-6, atol=0):
+        return False
+    top = np.take_along_axis(q8, np.abs(q32).argmax(-1)[..., None], -1)[..., 0] & 0x7F
+    if not np.all(top == 0x7E):
+        return False
+    dec = oracle.e4m3_to_f64(q8)
+    mag = np.maximum(np.abs(dec), 2.0 ** -6)
+    half_step = np.exp2(np.floor(np.log2(mag)) - 4)      # half the spacing: 3 mantissa bits
+    err = np.abs(dec * scale[..., None] - q32.astype(np.float64))
+    return bool(np.all(err <= half_step * scale[..., None] * (1 + 1e-5) + 1e-30))
+
+
+def test_quantize_properties_and_symmetries():
+    rng = np.random.default_rng(47)
+    R, H, D = 3, 64, 128
+    q32 = (rng.standard_normal((R, H, D)) * np.exp2(rng.integers(-6, 6, (R, H, 1)))).astype(np.float32)
+    q32 = torch.from_numpy(q32).to(torch.bfloat16).float().numpy()
+    w = rng.uniform(0.05, 1.0, (R, H)).astype(np.float32)
+    q8, wo = oracle.quantize_query(_bf16_bits(q32), w)
+    assert _quant_properties_hold(q32, w, q8, wo)
+    # negation flips the sign bits of the non-zero codes and keeps the weights
+    n8, nw = oracle.quantize_query(_bf16_bits(-q32), w)
+    nz = (q8 & 0x7F) != 0
+    assert np.array_equal(n8[nz], q8[nz] ^ 0x80) and np.array_equal(nw, wo)
+    # a power-of-two factor leaves the codes and scales the weights exactly
+    p8, pw = oracle.quantize_query(_bf16_bits(q32 * np.float32(2.0 ** -5)), w)
+    assert np.array_equal(p8, q8) and np.array_equal(pw, (wo * np.float32(2.0 ** -5)).astype(np.float32))
+
+
+def test_quantize_planted_mistake_is_caught():
+    """Codes from a wrong divisor (amax / 447) or weights missing the scale
+    fail the property check."""
+    rng = np.random.default_rng(48)
+    q32 = torch.from_numpy(rng.standard_normal((1, 8, 128)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    w = np.ones((1, 8), np.float32)
+    q8, wo = oracle.quantize_query(_bf16_bits(q32), w)
+    amax = np.abs(q32).max(-1, keepdims=True)
+    wrong = oracle.f32_to_e4m3((q32 / (amax / np.float32(447))).astype(np.float32))
+    assert not _quant_properties_hold(q32, w, wrong, wo)
+    assert not _quant_properties_hold(q32, w, q8, w)
