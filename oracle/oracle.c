@@ -313,14 +313,15 @@ int oracle_topk_rows(const float *scores, int64_t stride, const int32_t *lens, i
 
 /* The FP8 (E4M3) query of a bf16 index query, one scale per (row, head):
  * amax = the largest |q| of the head's elements, scale = amax / 448 in f32,
- * code = E4M3(q / scale) (f32 division, nearest-even rounding, saturated),
- * and the head weight w * scale in f32, so that w' * relu(code . k) equals
- * w * relu((code * scale) . k).  A head whose elements are all zero gets
- * scale 0: codes 0 and weight 0.  This is the per-token FP8 quantisation
- * "amax / 448, clamp, round to nearest even" that "[Perf] [MI355X] minimax_m31"
- * (section "Modifications", o_proj bullet) describes, applied per head to the
- * index query; the division is taken as one correctly rounded f32 division.
- * q and q8 are [R][H][D], head_w and w_out [R][H]. */
+ * inv = 1 / scale in f32, code = E4M3(q * inv) (f32 product, nearest-even
+ * rounding, saturated), and the head weight w * scale in f32, so that
+ * w' * relu(code . k) approximates w * relu(q . k).  A head whose elements
+ * are all zero gets scale 0: codes 0 and weight 0.  This is the per-token FP8
+ * quantisation that "[Perf] [MI355X] minimax_m31" (section "Modifications",
+ * o_proj bullet) describes -- amax / 448, a reciprocal, clamp, round to
+ * nearest even -- applied per head to the index query, with the reciprocal
+ * taken as a correctly rounded f32 division.  q and q8 are [R][H][D], head_w
+ * and w_out [R][H]. */
 void oracle_quantize_query(const uint16_t *q, const float *head_w, int R, int H, int D,
                            uint8_t *q8, float *w_out)
 {
@@ -335,10 +336,11 @@ void oracle_quantize_query(const uint16_t *q, const float *head_w, int R, int H,
                     amax = a;
             }
             const float scale = amax / 448.0f;
+            const float inv = scale > 0.0f ? 1.0f / scale : 0.0f;
             w_out[(size_t)r * H + h] = head_w[(size_t)r * H + h] * scale;
             for (int d = 0; d < D; ++d) {
                 const float x = (float)oracle_bf16_to_f64(row[d]);
-                out[d] = scale > 0.0f ? oracle_f32_to_e4m3(x / scale) : 0;
+                out[d] = scale > 0.0f ? oracle_f32_to_e4m3(x * inv) : 0;
             }
         }
 }
