@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-8k", action="store_true")
+    ap.add_argument("--no-fp8q", action="store_true", help="skip the FP8-query measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     return ap.parse_args()
 
@@ -193,15 +194,18 @@ class Step:
         self.idx = torch.zeros(self.R, self.k, dtype=torch.int32, device=dev)
         self.ws = binding.new_workspace(self.R, self.max_len, self.k, device=dev)
 
+    quantize_q = False  # score the on-device FP8 quantisation of the bf16 query
+
     def fused(self, c, stream=None):
         b = self.binding
         b.score_topk(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
                      self.seq_lens, self.row_req, self.max_len, self.k, self.idx, self.ws,
-                     scores=self.scores, stream=stream)
+                     scores=self.scores, stream=stream, quantize_q=self.quantize_q)
 
     def score_only(self, c, stream=None):
         self.binding.score(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
-                           self.seq_lens, self.row_req, self.scores, self.ws, stream=stream)
+                           self.seq_lens, self.row_req, self.scores, self.ws, stream=stream,
+                           quantize_q=self.quantize_q)
 
     def select_only(self, stream=None):
         self.binding.topk(self.scores, self.seq_lens, self.k, self.idx, self.ws, stream=stream)
@@ -468,6 +472,19 @@ def main():
         line["also_8k"] = {"workload": w8.recipe, "us": sec8 * 1e6,
                            "keys_per_s": w8.row_keys() / sec8}
         del st8
+    if not args.no_fp8q and not w.q_is_e4m3:
+        # the same workload with the query quantised to E4M3 on the device (one
+        # E4M3 term: half the MMAs); scores are those of the quantised query
+        st.quantize_q = True
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                st.fused(i, stream)
+            secq = time_graph_steps(st, min(args.steps, 4096), stream, None)
+            tq_score, _ = per_kernel_times(st, min(args.steps, 256), stream)
+        st.quantize_q = False
+        line["also_fp8_query"] = {"workload": w.recipe + "; query quantised to E4M3 on the device per (row, head)",
+                                  "us": secq * 1e6, "scoring_us": tq_score * 1e6,
+                                  "keys_per_s": w.row_keys() / secq}
     if not args.no_e2e:
         e2e_sec, h2d, d2h = e2e_time(st, min(args.steps, 200), stream)
         line["e2e"] = {"value": e2e_sec * 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,

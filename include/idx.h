@@ -58,15 +58,19 @@ typedef enum {
 } idx_status;
 
 typedef enum {
-    IDX_Q_BF16 = 0, /* q holds bf16 values */
-    IDX_Q_E4M3 = 1  /* q holds FP8 E4M3 codes; any per-(row, head) scale of q
-                       is the caller's to fold into head_w */
+    IDX_Q_BF16 = 0,     /* q holds bf16 values */
+    IDX_Q_E4M3 = 1,     /* q holds FP8 E4M3 codes; any per-(row, head) scale of q
+                           is the caller's to fold into head_w */
+    IDX_Q_BF16_FP8 = 2  /* q holds bf16 values that the scoring quantises to
+                           E4M3 on the device, one scale per (row, head) folded
+                           into head_w, as idx_quantize_query does; the scores
+                           are those of the quantised query */
 } idx_qtype;
 
 /* Bytes of workspace the calls below need for R rows, rows of at most
  * `max_len` keys and top-k size k.  `with_scores` != 0 adds room for an f32
  * score matrix [R][round_up(max_len, 4)], used by idx_score_topk when the
- * caller passes scores == NULL.  The workspace must be 256-byte aligned and
+ * caller passes scores == NULL.  The workspace must be 1024-byte aligned and
  * zeroed once before its first use (idx_workspace_init does that). */
 size_t idx_workspace_bytes(int R, int64_t max_len, int k, int with_scores);
 
@@ -76,7 +80,7 @@ idx_status idx_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 /*
  * idx_score -- score every key of each row's request against the row.
  *
- *  qtype        IDX_Q_BF16 or IDX_Q_E4M3
+ *  qtype        IDX_Q_BF16, IDX_Q_E4M3 or IDX_Q_BF16_FP8
  *  q            [R][IDX_HEADS][IDX_DIM] bf16 or E4M3, 16-byte aligned
  *  head_w       [R][IDX_HEADS] f32
  *  k_cache      [pool_pages][IDX_PAGE][IDX_DIM] E4M3 codes, 16-byte aligned
@@ -144,6 +148,27 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           int64_t max_len, int k, int32_t *indices,
                           float *scores, int64_t score_stride,
                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * idx_quantize_query -- the FP8 (E4M3) query of a bf16 index query, one scale
+ * per (row, head), as IDX_Q_BF16_FP8 scoring uses it.  The recipe is the
+ * per-token FP8 quantisation of "[Perf] [MI355X] minimax_m31" (section
+ * "Modifications", o_proj bullet) -- amax / 448, a reciprocal, clamp, round to
+ * nearest even -- applied per head: amax = max |q| over the head's IDX_DIM
+ * elements, scale = amax / 448 and inv = 1 / scale (correctly rounded f32
+ * divisions), q8 = E4M3(q * inv) (f32 product, nearest even, saturated at
+ * +-448); w_out = head_w * scale (f32).  A head whose elements are all zero gets
+ * codes 0 and weight 0.  Inputs are expected finite.
+ *
+ *  q       [R][IDX_HEADS][IDX_DIM] bf16, device, 8-byte aligned
+ *  head_w  [R][IDX_HEADS] f32, device
+ *  q8      [R][IDX_HEADS][IDX_DIM] E4M3 codes out, device, 4-byte aligned
+ *  w_out   [R][IDX_HEADS] f32 out, device
+ *
+ * Asynchronous on `stream`.  Errors: IDX_ERR_ARG, IDX_ERR_ALIGN, IDX_ERR_CUDA.
+ */
+idx_status idx_quantize_query(const void *q, const float *head_w, int R, uint8_t *q8, float *w_out,
+                              void *stream);
 
 /*
  * idx_host_workspace_bytes -- workspace bytes idx_score_topk_host needs for R

@@ -15,14 +15,14 @@ import torch
 from . import build as _build
 
 HEADS, DIM, PAGE, MAX_K, MAX_ROWS, GROUP_ROWS = 64, 128, 64, 2048, 1024, 4
-Q_BF16, Q_E4M3 = 0, 1
+Q_BF16, Q_E4M3, Q_BF16_FP8 = 0, 1, 2
 OK = 0
 STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORKSPACE",
           -4: "IDX_ERR_CUDA", -5: "IDX_ERR_TIMEOUT", -6: "IDX_ERR_BOUNDS", -7: "IDX_ERR_UNSUPPORTED"}
 
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
-           "idx_host_workspace_bytes", "idx_score_topk_host")
+           "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query")
 
 _lib = None
 
@@ -68,6 +68,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_version.argtypes = []
     lib.idx_score_noalloc.restype = i32
     lib.idx_score_noalloc.argtypes = score_common + [p, i64, p]
+    lib.idx_quantize_query.restype = i32
+    lib.idx_quantize_query.argtypes = [p, p, i32, p, p, p]
     lib.idx_host_workspace_bytes.restype = sz
     lib.idx_host_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
     lib.idx_score_topk_host.restype = i32
@@ -114,15 +116,33 @@ def new_workspace(R: int, max_len: int, k: int = MAX_K, with_scores: bool = Fals
     return ws
 
 
-def _qtype(q: torch.Tensor) -> int:
+def _qtype(q: torch.Tensor, quantize_q: bool = False) -> int:
     if q.dtype == torch.bfloat16:
-        return Q_BF16
+        return Q_BF16_FP8 if quantize_q else Q_BF16
     if q.dtype in (torch.uint8, torch.float8_e4m3fn):
+        if quantize_q:
+            raise ValueError("quantize_q needs a bfloat16 query")
         return Q_E4M3
     raise ValueError("q must be bfloat16 or E4M3 (uint8 / float8_e4m3fn)")
 
 
-def _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req):
+def quantize_query(q, head_w, q8=None, w_out=None, stream=None):
+    """idx_quantize_query: the FP8 query of a bf16 query [R, 64, 128], one
+    scale per (row, head) folded into the head weights.  Returns (q8 uint8
+    [R, 64, 128], w_out f32 [R, 64])."""
+    R = q.shape[0]
+    if q.dtype != torch.bfloat16 or tuple(q.shape) != (R, HEADS, DIM) or tuple(head_w.shape) != (R, HEADS):
+        raise ValueError("q must be bfloat16 [R, 64, 128] and head_w [R, 64]")
+    q8 = q8 if q8 is not None else torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    w_out = w_out if w_out is not None else torch.empty(head_w.shape, dtype=torch.float32, device=q.device)
+    st = load().idx_quantize_query(_dev(q, "q", torch.bfloat16), _dev(head_w, "head_w", torch.float32), int(R),
+                                   _dev(q8, "q8", torch.uint8), _dev(w_out, "w_out", torch.float32),
+                                   _stream(stream))
+    _check(st, "idx_quantize_query")
+    return q8, w_out
+
+
+def _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q=False):
     R = q.shape[0]
     if tuple(q.shape) != (R, HEADS, DIM) or tuple(head_w.shape) != (R, HEADS):
         raise ValueError("q must be [R, 64, 128] and head_w [R, 64]")
@@ -132,16 +152,18 @@ def _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req):
         raise ValueError("k_scale must be [pool_pages, 64]")
     if block_table.dim() != 2 or seq_lens.shape != (R,) or row_req.shape != (R,):
         raise ValueError("block_table [n_req, max_pages], seq_lens [R], row_req [R]")
-    return [_qtype(q), _dev(q, "q"), _dev(head_w, "head_w", torch.float32),
+    return [_qtype(q, quantize_q), _dev(q, "q"), _dev(head_w, "head_w", torch.float32),
             _dev(k_cache, "k_cache", (torch.uint8, torch.float8_e4m3fn)),
             _dev(k_scale, "k_scale", torch.float32), int(k_cache.shape[0]),
             _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
             _dev(seq_lens, "seq_lens", torch.int32), _dev(row_req, "row_req", torch.int32), int(R)]
 
 
-def score(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, workspace, stream=None):
-    """idx_score: scores[r, j] for j < seq_lens[r] (f32 [R, stride], stride % 4 == 0)."""
-    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
+def score(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, scores, workspace, stream=None,
+          quantize_q=False):
+    """idx_score: scores[r, j] for j < seq_lens[r] (f32 [R, stride], stride % 4 == 0).
+    quantize_q: score the on-device FP8 quantisation of a bf16 query."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
     if scores.dim() != 2 or scores.shape[0] != q.shape[0]:
         raise ValueError("scores must be [R, stride]")
     st = load().idx_score(*args, _dev(scores, "scores", torch.float32), int(scores.shape[1]),
@@ -175,10 +197,11 @@ def topk(scores, row_lens, k, indices, workspace=None, stream=None):
 
 
 def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
-               workspace, scores=None, stream=None):
+               workspace, scores=None, stream=None, quantize_q=False):
     """idx_score_topk: scoring then selection on one stream.  With scores=None
-    the scores live in the workspace (size it with with_scores=True)."""
-    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req)
+    the scores live in the workspace (size it with with_scores=True).
+    quantize_q: score the on-device FP8 quantisation of a bf16 query."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
     if indices.shape != (q.shape[0], k):
         raise ValueError("indices must be [R, k]")
     sp = _dev(scores, "scores", torch.float32) if scores is not None else None
@@ -217,7 +240,7 @@ def _host(t: torch.Tensor, name: str, dtype=None) -> int:
 
 
 def score_topk_host(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
-                    workspace, stream=None):
+                    workspace, stream=None, quantize_q=False):
     """idx_score_topk_host: q, head_w, block_table, seq_lens, row_req and the
     [R, k] indices are host tensors (pin them for asynchronous copies); the
     key cache, its scales and the workspace are device tensors.  Asynchronous:
@@ -230,7 +253,7 @@ def score_topk_host(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req,
     if block_table.dim() != 2 or seq_lens.shape != (R,) or row_req.shape != (R,) or indices.shape != (R, k):
         raise ValueError("block_table [n_req, max_pages], seq_lens/row_req [R], indices [R, k]")
     st = load().idx_score_topk_host(
-        _qtype(q), _host(q, "q"), _host(head_w, "head_w", torch.float32),
+        _qtype(q, quantize_q), _host(q, "q"), _host(head_w, "head_w", torch.float32),
         _dev(k_cache, "k_cache", (torch.uint8, torch.float8_e4m3fn)), _dev(k_scale, "k_scale", torch.float32),
         int(k_cache.shape[0]), _host(block_table, "block_table", torch.int32), int(block_table.shape[0]),
         int(block_table.shape[1]), _host(seq_lens, "seq_lens", torch.int32), _host(row_req, "row_req", torch.int32),

@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libidx.so")
-SOURCES = ["idx_api.cu", "score.cu", "select.cu", "stage.cu"]
-HEADERS = ["idx_internal.h", "ptx.cuh"]
+SOURCES = ["idx_api.cu", "score.cu", "select.cu", "stage.cu", "quant.cu"]
+HEADERS = ["idx_internal.h", "ptx.cuh", "quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

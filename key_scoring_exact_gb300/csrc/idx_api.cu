@@ -81,7 +81,7 @@ idx_status check_score_args(int qtype, const void* q, const float* head_w, const
                             const float* k_scale, int64_t pool_pages, const int32_t* block_table,
                             int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
                             void* workspace) {
-    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3 && qtype != IDX_Q_BF16_FP8) return IDX_ERR_ARG;
     if (!q || !head_w || !k_cache || !k_scale || !block_table || !seq_lens || !row_req) return IDX_ERR_ARG;
     if (R < 1 || R > kMaxRows) return IDX_ERR_ARG;
     if (pool_pages < 1 || pool_pages > (int64_t(1) << 25)) return IDX_ERR_ARG;
@@ -268,6 +268,17 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
     return to_status(launch_select(sel));
 }
 
+idx_status idx_quantize_query(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,
+                              void* stream) {
+    if (!q || !head_w || !q8 || !w_out) return IDX_ERR_ARG;
+    if (R < 1 || R > kMaxRows) return IDX_ERR_ARG;
+    if (!aligned(q, 8) || !aligned(head_w, 4) || !aligned(q8, 4) || !aligned(w_out, 4)) return IDX_ERR_ALIGN;
+    DeviceInfo dev;
+    const idx_status st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    return to_status(launch_quantize(q, head_w, R, q8, w_out, static_cast<cudaStream_t>(stream)));
+}
+
 size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int max_pages) {
     if (R < 1 || R > kMaxRows || max_len < 1 || k < 1 || k > IDX_MAX_K || n_req < 1 || max_pages < 1) return 0;
     return host_layout(R, max_len, k, n_req, max_pages).end;
@@ -280,7 +291,7 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
                                int32_t* indices_host, void* workspace, size_t ws_bytes, void* stream) {
     if (!q_host || !head_w_host || !block_table_host || !seq_lens_host || !row_req_host || !indices_host)
         return IDX_ERR_ARG;
-    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3 && qtype != IDX_Q_BF16_FP8) return IDX_ERR_ARG;
     if (R < 1 || R > kMaxRows || n_req < 1 || max_pages < 1 || k < 1 || k > IDX_MAX_K || max_len < 1)
         return IDX_ERR_ARG;
     if (!workspace) return IDX_ERR_WORKSPACE;
@@ -295,7 +306,7 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
         const void* host;
         size_t off, bytes;
     } in[kStageMaxCopies] = {
-        {q_host, H.q, (size_t)R * kHeads * kDim * (qtype == IDX_Q_BF16 ? 2 : 1)},
+        {q_host, H.q, (size_t)R * kHeads * kDim * (qtype == IDX_Q_E4M3 ? 1 : 2)},
         {head_w_host, H.w, (size_t)R * kHeads * 4},
         {block_table_host, H.bt, (size_t)n_req * (size_t)max_pages * 4},
         {seq_lens_host, H.lens, (size_t)R * 4},
@@ -369,7 +380,7 @@ idx_status idx_score_noalloc(int qtype, const void* q, const float* head_w, cons
                              float* scores, int64_t score_stride, void* stream) {
     if (R < 1 || R > IDX_NOALLOC_MAX_ROWS) return IDX_ERR_ARG;  // the static scratch holds this many rows
     // The checks of idx_score, minus the workspace (the scratch array is 256-byte aligned).
-    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3) return IDX_ERR_ARG;
+    if (qtype != IDX_Q_BF16 && qtype != IDX_Q_E4M3 && qtype != IDX_Q_BF16_FP8) return IDX_ERR_ARG;
     if (!q || !head_w || !k_cache || !k_scale || !block_table || !seq_lens || !row_req) return IDX_ERR_ARG;
     if (pool_pages < 1 || pool_pages > (int64_t(1) << 25)) return IDX_ERR_ARG;
     if (max_pages < 1 || (int64_t)max_pages * kPage > INT32_MAX) return IDX_ERR_ARG;

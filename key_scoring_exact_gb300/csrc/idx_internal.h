@@ -97,6 +97,10 @@ struct StagePlan {
     int n;
 };
 cudaError_t launch_stage(const StagePlan& plan, cudaStream_t stream);
+
+// FP8 query quantisation of a bf16 query [R][64][128] (quant.cuh).
+cudaError_t launch_quantize(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,
+                            cudaStream_t stream);
 // Longest row the selection handles with clusters of `cluster` CTAs.
 int64_t select_max_len(int cluster);
 constexpr int64_t kSelectMaxLen = 16 * 512 * 4 * 16;  // 524,288 keys (16-CTA clusters)

@@ -52,6 +52,7 @@
 
 #include "idx_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace idx {
 
@@ -218,12 +219,43 @@ __device__ __forceinline__ uint32_t swz_off(int n, int lane) {
 __device__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t* q_hi, uint8_t* q_lo,
                                   float* wq, int e, int lane) {
     const int pairs = nr * kHeads;
-    if (p.qtype == IDX_Q_E4M3) {
-        for (int pp = e; pp < pairs; pp += kEpiWarps) {
-            const int64_t src = (int64_t)r0 * kHeads + pp;
-            const uint32_t v = reinterpret_cast<const uint32_t*>(p.q)[src * 32 + lane];
-            *reinterpret_cast<uint32_t*>(q_hi + swz_off(pp, lane)) = v;
-            if (lane == 0) wq[pp] = p.head_w[src];
+    if (p.qtype != IDX_Q_BF16) {
+        // One E4M3 term: the query's codes as given (IDX_Q_E4M3), or quantised
+        // here with the scale folded into w' (IDX_Q_BF16_FP8).  A warp's pairs
+        // are loaded eight at a time.
+        constexpr int kBatch1 = 8;
+        const bool quant = p.qtype == IDX_Q_BF16_FP8;
+        for (int p0 = e; p0 < pairs; p0 += kEpiWarps * kBatch1) {
+            uint2 raw[kBatch1];
+            float wv[kBatch1];
+#pragma unroll
+            for (int b = 0; b < kBatch1; ++b) {
+                const int pp = p0 + b * kEpiWarps;
+                raw[b] = make_uint2(0, 0);
+                wv[b] = 0.0f;
+                if (pp < pairs) {
+                    const int64_t src = (int64_t)r0 * kHeads + pp;
+                    if (quant)
+                        raw[b] = reinterpret_cast<const uint2*>(p.q)[src * 32 + lane];
+                    else
+                        raw[b].x = reinterpret_cast<const uint32_t*>(p.q)[src * 32 + lane];
+                    wv[b] = p.head_w[src];
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch1; ++b) {
+                const int pp = p0 + b * kEpiWarps;
+                if (pp >= pairs) break;  // warp-uniform
+                uint32_t codes = raw[b].x;
+                float wq_b = wv[b];
+                if (quant) {
+                    float scale;
+                    codes = quantize_head_lane(raw[b], &scale);
+                    wq_b = __fmul_rn(wv[b], scale);
+                }
+                *reinterpret_cast<uint32_t*>(q_hi + swz_off(pp, lane)) = codes;
+                if (lane == 0) wq[pp] = wq_b;
+            }
         }
         return;
     }
@@ -419,7 +451,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t a0 = smem_u32(stages), bh = smem_u32(q_hi), bl = smem_u32(q_lo);
-            const int nmma = p.qtype == IDX_Q_BF16 ? 8 : 4;
+            const int nmma = p.qtype == IDX_Q_BF16 ? 8 : 4;  // hi and lo terms, or one E4M3 term
             int g = find_group(pl, n_groups, it0), qi = 0;
             int gend = -1;  // first work item past the current group
             uint32_t idesc = 0;
