@@ -204,6 +204,11 @@ __device__ __forceinline__ float e4m3_to_float(uint16_t codes, int which) {
     return __half2float(__half(h));
 }
 
+// 2 ReLU(x) = x + |x|: one add (the absolute value is an operand modifier)
+// on the FMA pipe instead of a max on the half-rate ALU pipe; exact, and a NaN
+// passes through as it does in the definition's ReLU.
+__device__ __forceinline__ float relu2(float x) { return __fadd_rn(x, fabsf(x)); }
+
 __device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]: exact 2^e
     return __int_as_float((e + 127) << 23);
 }
@@ -534,15 +539,16 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                     for (int h = 0; h < 32; h += 8) {
                         const float4 w0 = *reinterpret_cast<const float4*>(w + 32 * hf + h);
                         const float4 w1 = *reinterpret_cast<const float4*>(w + 32 * hf + h + 4);
-                        a[0] = ffma2(pack2(w0.x, w0.y), pack2(fmaxf(v[h + 0], 0.0f), fmaxf(v[h + 1], 0.0f)), a[0]);
-                        a[1] = ffma2(pack2(w0.z, w0.w), pack2(fmaxf(v[h + 2], 0.0f), fmaxf(v[h + 3], 0.0f)), a[1]);
-                        a[2] = ffma2(pack2(w1.x, w1.y), pack2(fmaxf(v[h + 4], 0.0f), fmaxf(v[h + 5], 0.0f)), a[2]);
-                        a[3] = ffma2(pack2(w1.z, w1.w), pack2(fmaxf(v[h + 6], 0.0f), fmaxf(v[h + 7], 0.0f)), a[3]);
+                        a[0] = ffma2(pack2(w0.x, w0.y), pack2(relu2(v[h + 0]), relu2(v[h + 1])), a[0]);
+                        a[1] = ffma2(pack2(w0.z, w0.w), pack2(relu2(v[h + 2]), relu2(v[h + 3])), a[1]);
+                        a[2] = ffma2(pack2(w1.x, w1.y), pack2(relu2(v[h + 4]), relu2(v[h + 5])), a[2]);
+                        a[3] = ffma2(pack2(w1.z, w1.w), pack2(relu2(v[h + 6]), relu2(v[h + 7])), a[3]);
                     }
                 }
                 const float2 s0 = unpack2(a[0]), s1 = unpack2(a[1]), s2 = unpack2(a[2]), s3 = unpack2(a[3]);
                 const float sum = ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
-                const float out = __fadd_rn(sum * sc, 0.0f);  // -0 -> +0
+                // the terms carry 2 ReLU(d): halve the sum (exact), then the scale
+                const float out = __fadd_rn((sum * 0.5f) * sc, 0.0f);  // -0 -> +0
                 if (pos < rlen) p.scores[(int64_t)(r0 + rr) * p.score_stride + pos] = out;
             }
             tc_fence_before_sync();
