@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-8k", action="store_true")
     ap.add_argument("--no-fp8q", action="store_true", help="skip the FP8-query measurement")
+    ap.add_argument("--no-batch", action="store_true", help="skip the 64-row measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     return ap.parse_args()
 
@@ -472,6 +473,20 @@ def main():
         line["also_8k"] = {"workload": w8.recipe, "us": sec8 * 1e6,
                            "keys_per_s": w8.row_keys() / sec8}
         del st8
+    if not args.no_batch:
+        # batch context: 16 requests x 4 verify rows (64 rows, 277 MB of keys)
+        wb = W.make_config(5)
+        stb = Step(wb, copies_for(wb, 2), dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                stb.fused(i, stream)
+            secb = time_graph_steps(stb, min(args.steps, 64), stream, None)
+            tb_score, tb_select = per_kernel_times(stb, min(args.steps, 32), stream)
+        line["also_64_rows"] = {"workload": wb.recipe, "us": secb * 1e6, "scoring_us": tb_score * 1e6,
+                                "selection_us": tb_select * 1e6,
+                                "scoring_gbs_of_keys": wb.unique_key_bytes() / tb_score / 1e9,
+                                "keys_per_s": wb.row_keys() / secb}
+        del stb
     if not args.no_fp8q and not w.q_is_e4m3:
         # the same workload with the query quantised to E4M3 on the device (one
         # E4M3 term: half the MMAs); scores are those of the quantised query

@@ -450,42 +450,76 @@ cudaError_t launch_c(const SelectArgs& a) {
                               a.status, cap);
 }
 
-bool cluster16_supported() {
-    static int ok = -1;
-    if (ok < 0) {
+// Clusters of CL CTAs (slices of `cap` keys) that can be resident at once on
+// this device; 0 when the size is refused.  Cached per (device, CL, cap).
+template <int CL>
+int max_active_clusters(int cap) {
+    static int cached_dev = -1, cached_cap = -1, cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev == cached_dev && cap == cached_cap) return cached;
+    int n = 0;
+    cudaError_t e = configure<CL>(dev);
+    if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(16, 1, 1);
+        cfg.gridDim = dim3(CL, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = slice_bytes(cap);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.x = CL;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int nclusters = 0, dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = configure<16>(dev);
-        cfg.dynamicSmemBytes = slice_bytes(kSliceCapMax);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&nclusters, k_select<16>, &cfg);
-        ok = (e == cudaSuccess && nclusters > 0) ? 1 : 0;
-        (void)cudaGetLastError();  // a refused query leaves no sticky error
+        e = cudaOccupancyMaxActiveClusters(&n, k_select<CL>, &cfg);
     }
-    return ok == 1;
+    if (e != cudaSuccess) n = 0;
+    (void)cudaGetLastError();  // a refused query leaves no sticky error
+    cached_dev = dev;
+    cached_cap = cap;
+    cached = n;
+    return n;
 }
 
 }  // namespace
 
 int64_t select_max_len(int cluster) { return (int64_t)cluster * kSliceCapMax; }
 
+// The cluster size: the largest of 16, 8, 4, 2, 1 CTAs whose slices hold the
+// longest row and whose clusters for all rows are resident at once; when no
+// size fits the rows in one wave, the smallest size that holds the row (the
+// most rows at once).  A row's slices then do more work each, but every CTA's
+// time is mostly fixed latencies (barriers, exchanges), so fewer waves win.
 cudaError_t launch_select(const SelectArgs& a) {
-    if (cluster16_supported()) {
-        if (a.max_len > select_max_len(16)) return cudaErrorInvalidValue;
-        return launch_c<16>(a);
+    int chosen = 0;
+    const int sizes[] = {16, 8, 4, 2, 1};
+    for (int cl : sizes) {
+        if (a.max_len > select_max_len(cl)) break;  // smaller clusters cannot hold the row either
+        const int cap = slice_cap_for(cl, a.max_len);
+        int active = 0;
+        switch (cl) {
+            case 16: active = max_active_clusters<16>(cap); break;
+            case 8: active = max_active_clusters<8>(cap); break;
+            case 4: active = max_active_clusters<4>(cap); break;
+            case 2: active = max_active_clusters<2>(cap); break;
+            default: active = max_active_clusters<1>(cap); break;
+        }
+        if (active <= 0) continue;  // size refused on this device
+        chosen = cl;
+        if (a.R <= active) break;
     }
-    if (a.max_len > select_max_len(8)) return cudaErrorInvalidValue;
-    return launch_c<8>(a);
+    switch (chosen) {
+        case 16: return launch_c<16>(a);
+        case 8: return launch_c<8>(a);
+        case 4: return launch_c<4>(a);
+        case 2: return launch_c<2>(a);
+        case 1: return launch_c<1>(a);
+        default: return cudaErrorInvalidValue;  // no cluster size holds the row
+    }
 }
 
 }  // namespace idx
