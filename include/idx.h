@@ -150,6 +150,24 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_score_topk_slots -- idx_score_topk whose lists hold physical cache
+ * slots instead of logical positions: a list entry for position p of row r
+ * is block_table[row_req[r]][p / IDX_PAGE] * IDX_PAGE + p % IDX_PAGE, the
+ * row of the paged key cache that holds the key, which is what a sparse
+ * attention over the same paged cache gathers ("sgl-amd-mono-upstream PR 18",
+ * the consumer's slot format); -1 padding stays -1.  The list order, the
+ * arguments and the errors are those of idx_score_topk (slots in place of
+ * indices).
+ */
+idx_status idx_score_topk_slots(int qtype, const void *q, const float *head_w,
+                                const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                                const int32_t *block_table, int max_pages,
+                                const int32_t *seq_lens, const int32_t *row_req, int R,
+                                int64_t max_len, int k, int32_t *slots,
+                                float *scores, int64_t score_stride,
+                                void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_quantize_query -- the FP8 (E4M3) query of a bf16 index query, one scale
  * per (row, head), as IDX_Q_BF16_FP8 scoring uses it.  The recipe is the
  * per-token FP8 quantisation of "[Perf] [MI355X] minimax_m31" (section

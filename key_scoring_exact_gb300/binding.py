@@ -22,7 +22,7 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
 
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
-           "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query")
+           "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots")
 
 _lib = None
 
@@ -60,6 +60,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_topk.argtypes = [p, i64, p, i32, i32, p, p, sz, p]
     lib.idx_score_topk.restype = i32
     lib.idx_score_topk.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
+    lib.idx_score_topk_slots.restype = i32
+    lib.idx_score_topk_slots.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
     lib.idx_check_status.restype = i32
     lib.idx_check_status.argtypes = [p, p]
     lib.idx_status_str.restype = ctypes.c_char_p
@@ -197,19 +199,20 @@ def topk(scores, row_lens, k, indices, workspace=None, stream=None):
 
 
 def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
-               workspace, scores=None, stream=None, quantize_q=False):
+               workspace, scores=None, stream=None, quantize_q=False, slots=False):
     """idx_score_topk: scoring then selection on one stream.  With scores=None
     the scores live in the workspace (size it with with_scores=True).
-    quantize_q: score the on-device FP8 quantisation of a bf16 query."""
+    quantize_q: score the on-device FP8 quantisation of a bf16 query.
+    slots: the lists hold physical cache slots (idx_score_topk_slots)."""
     args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
     if indices.shape != (q.shape[0], k):
         raise ValueError("indices must be [R, k]")
     sp = _dev(scores, "scores", torch.float32) if scores is not None else None
     stride = int(scores.shape[1]) if scores is not None else 0
-    st = load().idx_score_topk(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
-                               stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-                               _stream(stream))
-    _check(st, "idx_score_topk")
+    fn = load().idx_score_topk_slots if slots else load().idx_score_topk
+    st = fn(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
+            stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "idx_score_topk_slots" if slots else "idx_score_topk")
 
 
 def host_workspace_bytes(R: int, max_len: int, k: int, n_req: int, max_pages: int) -> int:

@@ -179,6 +179,48 @@ const void* mapped(const void* host) {
 }
 }  // namespace
 
+// The fused call; with `slots` the lists hold physical cache slots.
+static idx_status score_topk_impl(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                          const float* k_scale, int64_t pool_pages, const int32_t* block_table, int max_pages,
+                          const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
+                          int32_t* indices, float* scores, int64_t score_stride, void* workspace,
+                          size_t ws_bytes, void* stream, bool slots) {
+    idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
+                                     seq_lens, row_req, R, workspace);
+    if (st != IDX_OK) return st;
+    if (!indices || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
+    const int64_t cap = (int64_t)max_pages * kPage;
+    if (max_len > cap) max_len = cap;
+    if (max_len > kSelectMaxLen) return IDX_ERR_ARG;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != IDX_OK) return st;
+    const int with_scores = scores == nullptr;
+    const WsLayout L = ws_layout(R, max_len, with_scores);
+    if (ws_bytes < L.end) return IDX_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    if (with_scores) {
+        scores = reinterpret_cast<float*>(ws + L.scores);
+        score_stride = L.score_stride;
+    } else {
+        if (score_stride < max_len || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
+    st = run_score(a);
+    if (st != IDX_OK) return st;
+    // Each row's selection covers the keys its scores were written for.
+    SelectArgs sel{scores, score_stride, seq_lens, R, k, indices,
+                   reinterpret_cast<uint32_t*>(ws + L.status), max_len, max_len, s};
+    if (slots) {
+        sel.slot_table = block_table;
+        sel.slot_row_req = row_req;
+        sel.slot_max_pages = max_pages;
+    }
+    return to_status(launch_select(sel));
+}
+
 extern "C" {
 
 size_t idx_workspace_bytes(int R, int64_t max_len, int k, int with_scores) {
@@ -237,35 +279,17 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
                           const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
                           size_t ws_bytes, void* stream) {
-    idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
-                                     seq_lens, row_req, R, workspace);
-    if (st != IDX_OK) return st;
-    if (!indices || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
-    const int64_t cap = (int64_t)max_pages * kPage;
-    if (max_len > cap) max_len = cap;
-    if (max_len > kSelectMaxLen) return IDX_ERR_ARG;
-    DeviceInfo dev;
-    st = device_info(&dev);
-    if (st != IDX_OK) return st;
-    const int with_scores = scores == nullptr;
-    const WsLayout L = ws_layout(R, max_len, with_scores);
-    if (ws_bytes < L.end) return IDX_ERR_WORKSPACE;
-    char* ws = static_cast<char*>(workspace);
-    if (with_scores) {
-        scores = reinterpret_cast<float*>(ws + L.scores);
-        score_stride = L.score_stride;
-    } else {
-        if (score_stride < max_len || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
-                R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
-    st = run_score(a);
-    if (st != IDX_OK) return st;
-    // Each row's selection covers the keys its scores were written for.
-    SelectArgs sel{scores, score_stride, seq_lens, R, k, indices,
-                   reinterpret_cast<uint32_t*>(ws + L.status), max_len, max_len, s};
-    return to_status(launch_select(sel));
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false);
+}
+
+idx_status idx_score_topk_slots(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                                const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                                int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                                int64_t max_len, int k, int32_t* slots, float* scores, int64_t score_stride,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, slots, scores, score_stride, workspace, ws_bytes, stream, true);
 }
 
 idx_status idx_quantize_query(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,

@@ -80,6 +80,11 @@ struct SelectArgs {
     int64_t max_len;      // bound on row lengths (launch shape)
     int64_t len_cap;      // rows longer than this are cut to it (and reported)
     cudaStream_t stream;
+    // When slot_table is set, list entries are physical cache slots
+    // (slot_table[row_req[r]][pos / page] * page + pos % page) instead of positions.
+    const int32_t* slot_table = nullptr;
+    const int32_t* slot_row_req = nullptr;
+    int slot_max_pages = 0;
 };
 
 cudaError_t launch_select(const SelectArgs& a);

@@ -231,10 +231,21 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
     __syncthreads();
 }
 
+// List entries as positions, or as physical cache slots of the row's request.
+struct SlotMap {
+    const int32_t* table;    // [n_req][max_pages] page ids, or null for positions
+    const int32_t* row_req;  // [R]
+    int max_pages;
+};
+
+__device__ __forceinline__ int32_t list_entry(const int32_t* page_row, int64_t pos) {
+    return page_row ? page_row[pos / kPage] * kPage + (int32_t)(pos % kPage) : (int32_t)pos;
+}
+
 template <int CL>
 __global__ void __launch_bounds__(kThreads)
 k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __restrict__ row_lens,
-         int64_t stride, int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap) {
+         int64_t stride, int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap, SlotMap sm) {
     extern __shared__ __align__(16) uint32_t keys_s[];  // slice_cap radix keys (+ 4)
     __shared__ Shared S;
     const uint32_t c = cluster_ctarank();
@@ -267,9 +278,10 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         n = (int64_t)CL * slice_cap;
     }
     int32_t* dst = out + (int64_t)row * k;
+    const int32_t* page_row = sm.table ? sm.table + (int64_t)sm.row_req[row] * sm.max_pages : nullptr;
     if (n <= k) {  // uniform over the cluster: no barrier is skipped by a subset
         if (c == 0)
-            for (int j = tid; j < k; j += kThreads) dst[j] = j < n ? j : -1;
+            for (int j = tid; j < k; j += kThreads) dst[j] = j < n ? list_entry(page_row, j) : -1;
         return;
     }
     const bool single = n <= slice_cap;
@@ -383,10 +395,10 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
                 const int i = 4 * j + q;
                 if (i >= cnt) break;
                 if (uu[q] > T) {
-                    if (pg < gt_total) dst[pg] = (int32_t)(start + i);
+                    if (pg < gt_total) dst[pg] = list_entry(page_row, start + i);
                     ++pg;
                 } else if (uu[q] == T) {
-                    if (pe < (uint32_t)k) dst[pe] = (int32_t)(start + i);
+                    if (pe < (uint32_t)k) dst[pe] = list_entry(page_row, start + i);
                     ++pe;
                 }
             }
@@ -446,8 +458,9 @@ cudaError_t launch_c(const SelectArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int64_t cap_len = a.len_cap < a.score_stride ? a.len_cap : a.score_stride;
+    const SlotMap sm{a.slot_table, a.slot_row_req, a.slot_max_pages};
     return cudaLaunchKernelEx(&cfg, k_select<CL>, a.scores, cap_len, a.row_lens, a.score_stride, a.k, a.indices,
-                              a.status, cap);
+                              a.status, cap, sm);
 }
 
 // Clusters of CL CTAs (slices of `cap` keys) that can be resident at once on

@@ -66,6 +66,8 @@ def _load():
             lib.oracle_topk_rows.argtypes = [p, i64, p, i32, i32, p]
             lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
             lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_slots.restype = None
+            lib.oracle_slots.argtypes = [p, i32, i32, p, i32, p, i32, p]
             lib.oracle_quantize_query.restype = None
             lib.oracle_quantize_query.argtypes = [p, p, i32, i32, i32, p, p]
             _lib = lib
@@ -125,6 +127,17 @@ def quantize_query(q_bits, head_w):
     wo = np.empty((R, H), np.float32)
     lib.oracle_quantize_query(_ptr(q), _ptr(w), R, H, D, _ptr(q8), _ptr(wo))
     return q8, wo
+
+
+def slots(idx, block_table, row_req, page: int = 64) -> np.ndarray:
+    """Logical positions [R, k] (-1 = padding) as physical cache slots."""
+    lib = _load()
+    i = _c(idx, np.int32)
+    bt = _c(block_table, np.int32)
+    rr = _c(row_req, np.int32)
+    out = np.empty(i.shape, np.int32)
+    lib.oracle_slots(_ptr(i), i.shape[0], i.shape[1], _ptr(bt), bt.shape[1], _ptr(rr), int(page), _ptr(out))
+    return out
 
 
 class Problem:

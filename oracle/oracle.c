@@ -344,3 +344,20 @@ void oracle_quantize_query(const uint16_t *q, const float *head_w, int R, int H,
             }
         }
 }
+
+/* ------------------------------------------------------- physical slots */
+
+/* A list of logical positions as rows of the paged key cache: position p of
+ * row r lives in page block_table[row_req[r]][p / page], row p % page of it,
+ * i.e. cache slot page_id * page + p % page; -1 (padding) stays -1.
+ * idx and out are [R][k]. */
+void oracle_slots(const int32_t *idx, int R, int k, const int32_t *block_table, int max_pages,
+                  const int32_t *row_req, int page, int32_t *out)
+{
+    for (int r = 0; r < R; ++r)
+        for (int j = 0; j < k; ++j) {
+            const int32_t p = idx[(size_t)r * k + j];
+            out[(size_t)r * k + j] =
+                p < 0 ? -1 : block_table[(size_t)row_req[r] * max_pages + p / page] * page + p % page;
+        }
+}

@@ -115,3 +115,20 @@ def test_host_buffer_call_matches_device_call(cfg, pinned):
     torch.cuda.synchronize()
     assert binding.check_status(ws) == 0
     assert np.array_equal(out.numpy(), ref)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_slot_lists(cfg):
+    """idx_score_topk_slots: the same lists as idx_score_topk, each position
+    replaced by its physical cache slot (the oracle's mapping)."""
+    w = W.make_config(cfg)
+    t = device_inputs(w)
+    _, pos, st = gpu_fused(w, t)
+    assert st == 0
+    got = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+    ws = binding.new_workspace(w.R, w.max_len, w.k, with_scores=True)
+    binding.score_topk(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"], t["seq_lens"],
+                       t["row_req"], w.max_len, w.k, got, ws, slots=True)
+    assert binding.check_status(ws) == 0
+    want = oracle.slots(pos, w.block_table.numpy(), w.row_req.numpy())
+    assert np.array_equal(got.cpu().numpy(), want)

@@ -484,3 +484,19 @@ def test_quantize_planted_mistake_is_caught():
     wrong = oracle.f32_to_e4m3((q32 / (amax / np.float32(447))).astype(np.float32))
     assert not _quant_properties_hold(q32, w, wrong, wo)
     assert not _quant_properties_hold(q32, w, q8, w)
+
+
+# ---------------------------------------------------------------- physical slots
+
+def test_slots_worked_example_and_closed_forms():
+    """Pages of 64 keys: request 0's block table [5, 2, 9] puts position 0 in
+    slot 5 * 64 = 320, position 63 in 383, position 64 in page 2 (slot 128)
+    and position 130 in page 9 at row 2 (slot 578); an identity table maps
+    every position to itself; padding stays -1."""
+    bt = np.array([[5, 2, 9], [0, 1, 2]], np.int32)
+    idx = np.array([[0, 63, 64, 130, -1], [0, 63, 64, 130, -1]], np.int32)
+    got = oracle.slots(idx, bt, np.array([0, 1], np.int32))
+    assert got.tolist() == [[320, 383, 128, 578, -1], [0, 63, 64, 130, -1]]
+    ident = np.arange(64, dtype=np.int32)[None, :]
+    pos = np.random.default_rng(3).integers(0, 64 * 64, (3, 50)).astype(np.int32)
+    assert np.array_equal(oracle.slots(pos, ident, np.zeros(3, np.int32)), pos)
