@@ -8,27 +8,32 @@
 // digit holding the remaining k-th key and the count above it follow.
 //
 // GB300 form:
-//  * A row is one thread-block cluster (16 CTAs, else 8).  The slices are the
-//    cluster's CTAs; a row short enough for one slice runs on one CTA alone.
-//  * A slice's keys live in shared memory (loaded with float4 reads issued
-//    together), as the order-preserving uint32 image of the f32 score (-0
-//    folded into +0, NaN below every number).  The rounds run one compact
-//    loop body, so a one-shot launch does not refetch unrolled code.
+//  * A row is one thread-block cluster of 16, 8, 4, 2 or 1 CTAs, the size
+//    chosen per launch (the largest whose slices hold the longest row and
+//    whose clusters for all rows are resident at once).  The slices are the
+//    cluster's CTAs; slice c covers positions [c P, (c + 1) P) with P fixed by
+//    the launch's length bound, so its score loads go out together with the
+//    read of the row's length; a row of at most P keys runs on one CTA alone.
+//  * A slice's keys live in shared memory, as the order-preserving uint32
+//    image of the f32 score (-0 folded into +0, NaN below every number).
 //  * Digits of 11, 11 and 10 bits: three rounds give the exact k-th largest
 //    image T and the number kr of keys equal to T that the list takes.  The
 //    first round's histogram is built while the slice is loaded.
 //  * Histograms are built in shared memory with plain atomic adds (on this
 //    hardware faster than aggregating equal digits within a warp first, even
-//    when the scores crowd into a few bins); each slice then adds its
-//    non-zero bins into every slice's own totals with distributed-shared-
-//    memory reductions, so after one hardware cluster barrier each slice
-//    scans its local totals.  No slice spins on another; every wait is a
-//    cluster barrier.
+//    when the scores crowd into a few bins).  The slices' histograms are
+//    summed by reduce-scatter and all-gather: bin b belongs to slice
+//    b / (bins / slices), every slice adds its non-zero bins there with a
+//    distributed-shared-memory reduction, and after one hardware cluster
+//    barrier each thread reads its four bins' totals from their owner with
+//    one 16-byte remote load, then the block scans them.  No slice spins on
+//    another; every wait is a cluster barrier.
 //  * Each thread then owns a contiguous run of the slice's positions: one
 //    block scan of its packed (above T, at T) counts gives its offsets within
-//    the slice, each slice adds its totals into every later slice, and after
-//    one more barrier the positions are written in order: keys above T
-//    first, then ties, each in ascending position.
+//    the slice, each slice stores its totals into every later slice, and
+//    after one more barrier the positions are written in order: keys above T
+//    first, then ties, each in ascending position (or, for the slot variant,
+//    the cache slots those positions map to).
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -36,10 +41,7 @@ namespace idx {
 
 namespace {
 
-#ifndef IDX_SELECT_THREADS
-#define IDX_SELECT_THREADS 1024
-#endif
-constexpr int kThreads = IDX_SELECT_THREADS;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 static_assert(kThreads >= 256 && kThreads <= 1024 && kThreads % 256 == 0, "block size");
 constexpr int kLoadUnroll = 4096 / kThreads;  // float4 reads in flight per thread (16K keys a CTA)
