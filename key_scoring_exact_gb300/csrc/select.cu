@@ -504,15 +504,20 @@ int max_active_clusters(int cap) {
 
 int64_t select_max_len(int cluster) { return (int64_t)cluster * kSliceCapMax; }
 
-// The cluster size: the largest of 16, 8, 4, 2, 1 CTAs whose slices hold the
-// longest row and whose clusters for all rows are resident at once; when no
+// The cluster size: the largest of 16, 8, 4, 2, 1 CTAs, but no more than the
+// longest row's slices of kSliceTarget keys, whose slices hold the longest
+// row and whose clusters for all rows are resident at once; when no
 // size fits the rows in one wave, the smallest size that holds the row (the
 // most rows at once).  A row's slices then do more work each, but every CTA's
 // time is mostly fixed latencies (barriers, exchanges), so fewer waves win.
 cudaError_t launch_select(const SelectArgs& a) {
     int chosen = 0;
     const int sizes[] = {16, 8, 4, 2, 1};
+    // no more CTAs than the longest row has slices of kSliceTarget keys: extra
+    // CTAs would hold no keys yet take part in every cluster barrier
+    const int64_t want = (a.max_len + kSliceTarget - 1) / kSliceTarget;
     for (int cl : sizes) {
+        if (cl > 1 && (int64_t)(cl / 2) >= want) continue;
         if (a.max_len > select_max_len(cl)) break;  // smaller clusters cannot hold the row either
         const int cap = slice_cap_for(cl, a.max_len);
         int active = 0;

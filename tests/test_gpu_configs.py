@@ -132,3 +132,19 @@ def test_slot_lists(cfg):
     assert binding.check_status(ws) == 0
     want = oracle.slots(pos, w.block_table.numpy(), w.row_req.numpy())
     assert np.array_equal(got.cpu().numpy(), want)
+
+
+def test_host_buffer_call_e4m3_query():
+    """idx_score_topk_host with an E4M3 query (one byte per element)."""
+    w = W.make_workload([W.chain(5000)], "random", seed=91, q_is_e4m3=True)
+    t = device_inputs(w)
+    _, ref, st = gpu_fused(w, t)
+    assert st == 0
+    ws = binding.new_host_workspace(w.R, w.max_len, w.k, w.block_table.shape[0], w.block_table.shape[1])
+    out = torch.full((w.R, w.k), -7, dtype=torch.int32).pin_memory()
+    binding.score_topk_host(w.q.pin_memory(), w.head_w.pin_memory(), t["k_cache"], t["k_scale"],
+                            w.block_table.pin_memory(), w.seq_lens.pin_memory(), w.row_req.pin_memory(),
+                            w.max_len, w.k, out, ws)
+    torch.cuda.synchronize()
+    assert binding.check_status(ws) == 0
+    assert np.array_equal(out.numpy(), ref)
