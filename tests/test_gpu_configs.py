@@ -148,3 +148,25 @@ def test_host_buffer_call_e4m3_query():
     torch.cuda.synchronize()
     assert binding.check_status(ws) == 0
     assert np.array_equal(out.numpy(), ref)
+
+
+def test_most_rows():
+    """The largest row count (IDX_MAX_ROWS = 1,024 rows): 300 requests of 1 to
+    7 rows (groups of up to four, so many CTAs start in the middle of a
+    request), rows from 0 to 700 keys (k = 256), end to end through the fused
+    call."""
+    rng = np.random.default_rng(1024)
+    reqs, total = [], 0
+    while total < 1024:
+        nr = int(min(rng.integers(1, 8), 1024 - total))
+        base = int(rng.integers(0, 700))
+        reqs.append([max(0, base - j) for j in range(nr)][::-1])
+        total += nr
+    w = W.make_workload(reqs, "random", seed=1024, k=256, extra_pages=2)
+    assert w.R == 1024
+    s, got, st = gpu_fused(w)
+    assert st == 0
+    ref = oracle.scores(problem(w))
+    errs = checks.score_errors(s, ref, w.seq_lens.tolist())
+    assert max(errs) <= checks.SCORE_TOL
+    _lists_exact(w, s, got)

@@ -161,3 +161,15 @@ def test_deterministic_replays():
     for _ in range(5):
         b, _ = gpu_topk(s, [60000, 59999, 30000, 2049], 2048)
         assert np.array_equal(a, b)
+
+
+def test_longest_row():
+    """A row of the largest length the selection takes (IDX_MAX_TOPK_LEN =
+    524,288 keys: 16 slices of 32,768), plus a second row of half of it."""
+    rng = np.random.default_rng(524)
+    n = 524288
+    s = (rng.standard_normal((2, n)) * 3).astype(np.float32)
+    lens = [n, n // 2]
+    got, st = gpu_topk(s, lens, 2048)
+    assert st == 0
+    _check_rows(s, lens, 2048, got)
