@@ -535,6 +535,13 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 for (int hf = 0; hf < 2; ++hf) {
                     float v[32];
                     tmem_load_32cols(taddr + 32 * hf, v);
+                    if (hf == 1) {
+                        // every column of this warp is in registers: release the
+                        // accumulator before the second half's arithmetic
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                    }
 #pragma unroll
                     for (int h = 0; h < 32; h += 8) {
                         const float4 w0 = *reinterpret_cast<const float4*>(w + 32 * hf + h);
@@ -550,10 +557,11 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 // the terms carry 2 ReLU(d): halve the sum (exact), then the scale
                 const float out = __fadd_rn((sum * 0.5f) * sc, 0.0f);  // -0 -> +0
                 if (pos < rlen) p.scores[(int64_t)(r0 + rr) * p.score_stride + pos] = out;
+            } else {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
         }
     }
 
