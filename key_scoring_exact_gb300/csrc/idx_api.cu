@@ -36,9 +36,10 @@ struct DeviceInfo {
     int num_sms = 0;
 };
 
+// Cached per host thread, so concurrent callers share no mutable state.
 idx_status device_info(DeviceInfo* out) {
-    static DeviceInfo cache[64];
-    static int cached[64] = {0};
+    static thread_local DeviceInfo cache[64];
+    static thread_local int cached[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -577,7 +577,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
 }  // namespace
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
-    static int configured_device = -1;
+    static thread_local int configured_device = -1;  // per host thread: setting the attribute is idempotent
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;

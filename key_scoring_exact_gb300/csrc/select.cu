@@ -419,10 +419,11 @@ int slice_cap_for(int cl, int64_t max_len) {
 
 constexpr size_t slice_bytes(int cap) { return (size_t)((cap + 4 + 3) & ~3) * 4; }
 
-// Once per device: cluster and shared-memory attributes of k_select<CL>.
+// Once per device (and host thread: setting the attributes is idempotent):
+// cluster and shared-memory attributes of k_select<CL>.
 template <int CL>
 cudaError_t configure(int dev) {
-    static int configured_device = -1;
+    static thread_local int configured_device = -1;
     if (configured_device == dev) return cudaSuccess;
     cudaError_t err = cudaSuccess;
     if (CL > 8) {
@@ -466,10 +467,11 @@ cudaError_t launch_c(const SelectArgs& a) {
 }
 
 // Clusters of CL CTAs (slices of `cap` keys) that can be resident at once on
-// this device; 0 when the size is refused.  Cached per (device, CL, cap).
+// this device; 0 when the size is refused.  Cached per host thread and
+// (device, CL, cap).
 template <int CL>
 int max_active_clusters(int cap) {
-    static int cached_dev = -1, cached_cap = -1, cached = 0;
+    static thread_local int cached_dev = -1, cached_cap = -1, cached = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();

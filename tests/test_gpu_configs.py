@@ -170,3 +170,43 @@ def test_most_rows():
     errs = checks.score_errors(s, ref, w.seq_lens.tolist())
     assert max(errs) <= checks.SCORE_TOL
     _lists_exact(w, s, got)
+
+
+def test_concurrent_host_threads():
+    """Four host threads call the fused entry point at once, each on its own
+    stream and workspace (ctypes releases the GIL during the call): every
+    call returns the single-threaded lists."""
+    import threading
+    ws_cfg = [W.make_config(2), W.make_config(1)]
+    refs, inputs = [], []
+    for w in ws_cfg:
+        t = device_inputs(w)
+        _, ref, st = gpu_fused(w, t)
+        assert st == 0
+        refs.append(ref)
+        inputs.append((w, t))
+    errors = []
+
+    def worker(j):
+        try:
+            w, t = inputs[j % 2]
+            stream = torch.cuda.Stream()
+            ws = binding.new_workspace(w.R, w.max_len, w.k, with_scores=True)
+            for _ in range(20):
+                idx = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+                with torch.cuda.stream(stream):
+                    binding.score_topk(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"],
+                                       t["seq_lens"], t["row_req"], w.max_len, w.k, idx, ws, stream=stream)
+                stream.synchronize()
+                if binding.check_status(ws, stream) != 0 or not np.array_equal(idx.cpu().numpy(), refs[j % 2]):
+                    errors.append(j)
+                    return
+        except Exception as exc:  # reported below
+            errors.append(repr(exc))
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
