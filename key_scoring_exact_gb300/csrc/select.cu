@@ -199,35 +199,38 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
     uint32_t sum = 0;
 #pragma unroll
     for (int q = 0; q < kBptMax; ++q) sum += tv[q];
-    uint32_t incl = sum;
+    // The warps' totals, then only the warp whose prefix reaches kr scans its
+    // threads (digits run from the largest down in thread order).
+    const uint32_t wtot = __reduce_add_sync(kFull, sum);
+    if (lane == 0) S.wsum[warp] = wtot;
+    __syncthreads();
+    const uint32_t wv = lane < kWarps ? S.wsum[lane] : 0u;
+    uint32_t wi = wv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += x;
+        const uint32_t x = __shfl_up_sync(kFull, wi, o);
+        if (lane >= o) wi += x;
     }
-    if (lane == 31) S.wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {  // exclusive prefix of the warp totals
-        const uint32_t wv = lane < kWarps ? S.wsum[lane] : 0u;
-        uint32_t wi = wv;
+    const uint32_t wbefore = __shfl_sync(kFull, wi - wv, warp);
+    const uint32_t wafter = __shfl_sync(kFull, wi, warp);
+    if (wbefore < kr && wafter >= kr) {  // warp-uniform
+        uint32_t incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(kFull, wi, o);
-            if (lane >= o) wi += x;
+            const uint32_t x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
         }
-        if (lane < kWarps) S.wsum[lane] = wi - wv;
-    }
-    __syncthreads();
-    uint32_t above = S.wsum[warp] + incl - sum;
+        uint32_t above = wbefore + incl - sum;
 #pragma unroll
-    for (int q = kBptMax - 1; q >= 0; --q) {
-        if (q < bpt) {
-            if (above < kr && above + tv[q] >= kr) {
-                S.pick[0] = (uint32_t)(b0 + q);
-                S.pick[1] = above;
-                S.pick[2] = tv[q];
+        for (int q = kBptMax - 1; q >= 0; --q) {
+            if (q < bpt) {
+                if (above < kr && above + tv[q] >= kr) {
+                    S.pick[0] = (uint32_t)(b0 + q);
+                    S.pick[1] = above;
+                    S.pick[2] = tv[q];
+                }
+                above += tv[q];
             }
-            above += tv[q];
         }
     }
     __syncthreads();
