@@ -63,9 +63,8 @@ def test_tie_heavy(levels):
 
 def test_concentrated_values():
     """Every score in one quarter-binade: the first 11-bit digit leaves all
-    keys in one bin, so the threshold is found in the next digits (the rows
-    take the selection's later gather points and, with heavy ties, its
-    general tail)."""
+    keys in one bin, so the threshold comes from the two lower digits, whose
+    histograms hold every key of the row."""
     rng = np.random.default_rng(5)
     n = 100000
     lens = [n, n, n]
@@ -82,8 +81,7 @@ def test_concentrated_values():
 @pytest.mark.parametrize("n_tied", [1, 37, 300, 512, 513, 900])
 def test_ties_at_the_threshold(n_tied):
     """A few hundred keys equal to the k-th score, spread over every slice of a
-    long row: the threshold's last digit and the ties are resolved on keys
-    gathered after two digits (up to 512 of them), or by the general tail."""
+    long row: the list takes them in position order across the slices."""
     rng = np.random.default_rng(1000 + n_tied)
     n = 120000
     s = rng.standard_normal(n).astype(np.float32)
@@ -173,3 +171,30 @@ def test_longest_row():
     got, st = gpu_topk(s, lens, 2048)
     assert st == 0
     _check_rows(s, lens, 2048, got)
+
+
+
+@pytest.mark.parametrize("n", [20000, 131072])
+@pytest.mark.parametrize("placement", ["spread", "first_keys", "last_keys"])
+@pytest.mark.parametrize("c1", [600, 8192])
+def test_crowded_first_digit(n, placement, c1):
+    """c1 keys share the k-th key's first digit (scores in [1, 1.25)), 1,000
+    lie above it and the rest below; the crowded bin sits spread over the
+    row, in its first keys (one or two slices) or in its last keys, and a
+    few of its keys tie at the threshold."""
+    rng = np.random.default_rng(c1 + n + len(placement))
+    s = rng.uniform(0.1, 0.9, n).astype(np.float32)            # below the bin
+    if placement == "spread":
+        pos = rng.choice(n, 1000 + c1, replace=False)
+    elif placement == "first_keys":
+        pos = rng.permutation(1000 + c1)
+    else:
+        pos = n - 1 - rng.permutation(1000 + c1)
+    above, cand = pos[:1000], pos[1000:]
+    s[above] = rng.uniform(2.0, 4.0, 1000).astype(np.float32)  # above the bin
+    s[cand] = (1.0 + 0.2499 * rng.random(c1)).astype(np.float32)
+    v = np.sort(s)[::-1][2047]
+    s[cand[:17]] = v                                           # ties at the threshold
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
