@@ -211,6 +211,15 @@ size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int ma
  * it, or wait on an event recorded after the call), and the host must not
  * modify the inputs before then.
  *
+ * When every buffer is mapped and `stream` is an explicit stream that is not
+ * being captured, the call's launches run as one CUDA graph kept per host
+ * thread: the launches are captured from `stream`, written into the thread's
+ * executable graph (updated in place when only arguments change, else built
+ * again) and launched with cudaGraphLaunch.  The first such call of a thread
+ * launches directly.  Calls on the legacy or per-thread default stream, with
+ * a pageable buffer, or under a caller's capture launch directly.  Launches
+ * of one thread's graph run in order, whatever stream they are issued on.
+ *
  *  workspace  device memory, 1024-byte aligned, >= idx_host_workspace_bytes
  *             (R, max_len, k, n_req, max_pages), zeroed once by idx_workspace_init
  *

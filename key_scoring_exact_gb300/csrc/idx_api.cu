@@ -309,6 +309,117 @@ size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int ma
     return host_layout(R, max_len, k, n_req, max_pages).end;
 }
 
+namespace {
+// One host-buffer call: where each input goes in the workspace, which of
+// them the stage kernel gathers over the host link (page-locked, mapped
+// buffers) and which the copy engine copies, and where the indices go.
+struct HostCall {
+    int qtype, R, max_pages, k;
+    const uint8_t* k_cache;
+    const float* k_scale;
+    int64_t pool_pages, max_len;
+    char* ws;
+    size_t ws_bytes;
+    HostLayout H;
+    StagePlan plan;
+    struct {
+        const void* host;
+        size_t off, bytes;
+    } copy[kStageMaxCopies];  // inputs the copy engine takes
+    int n_copy;
+    int32_t* indices_host;
+    int32_t* idx_out;  // mapped host indices, or the workspace's (then copied back)
+};
+
+// Every launch and copy of one host-buffer call, in stream order.
+idx_status host_launches(const HostCall& c, cudaStream_t s) {
+    for (int i = 0; i < c.n_copy; ++i) {
+        if (cudaMemcpyAsync(c.ws + c.copy[i].off, c.copy[i].host, c.copy[i].bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return IDX_ERR_CUDA;
+        }
+    }
+    if (c.plan.n > 0 && launch_stage(c.plan, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    const HostLayout& H = c.H;
+    const idx_status st =
+        idx_score_topk(c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale,
+                       c.pool_pages, reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages,
+                       reinterpret_cast<const int32_t*>(c.ws + H.lens), reinterpret_cast<const int32_t*>(c.ws + H.rreq),
+                       c.R, c.max_len, c.k, c.idx_out, nullptr, 0, c.ws, c.ws_bytes, s);
+    if (st != IDX_OK) return st;
+    int32_t* idx_dev = reinterpret_cast<int32_t*>(c.ws + H.idx);
+    if (c.idx_out == idx_dev && cudaMemcpyAsync(c.indices_host, idx_dev, (size_t)c.R * (size_t)c.k * 4,
+                                                cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    return IDX_OK;
+}
+
+// A call whose buffers are all mapped host memory runs as one CUDA graph: its
+// launches are captured from the stream, written into this host thread's
+// executable graph (cudaGraphExecUpdate keeps it when only the arguments
+// changed) and launched with one cudaGraphLaunch, which starts the kernels
+// with less device-side delay than three stream launches.  The executable
+// graph is kept for the life of the thread.
+struct HostGraph {
+    int dev = -1;
+    bool warm = false;  // an eager call of this thread has set up every kernel's attributes
+    cudaGraphExec_t exec = nullptr;
+};
+thread_local HostGraph host_graph;
+
+idx_status host_launches_graph(const HostCall& c, cudaStream_t s, int dev) {
+    HostGraph& hg = host_graph;
+    if (hg.dev != dev) {  // another device: start over (the old graph stays with its context)
+        hg = HostGraph{};
+        hg.dev = dev;
+    }
+    if (!hg.warm) {
+        const idx_status st = host_launches(c, s);
+        if (st == IDX_OK) hg.warm = true;
+        return st;
+    }
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return host_launches(c, s);
+    }
+    const idx_status st = host_launches(c, s);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(s, &g);
+    if (st != IDX_OK || ec != cudaSuccess || g == nullptr) {
+        if (g) cudaGraphDestroy(g);
+        (void)cudaGetLastError();
+        if (st != IDX_OK) return st;  // an argument error: nothing was issued
+        return host_launches(c, s);   // the capture failed: run eagerly
+    }
+    if (hg.exec) {
+        cudaGraphExecUpdateResultInfo info;
+        if (cudaGraphExecUpdate(hg.exec, g, &info) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphExecDestroy(hg.exec);
+            hg.exec = nullptr;
+        }
+    }
+    if (!hg.exec && cudaGraphInstantiate(&hg.exec, g, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        hg.exec = nullptr;
+        cudaGraphDestroy(g);
+        return host_launches(c, s);
+    }
+    cudaGraphDestroy(g);
+    if (cudaGraphLaunch(hg.exec, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return IDX_ERR_CUDA;
+    }
+    return IDX_OK;
+}
+}  // namespace
+
 idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_w_host, const uint8_t* k_cache,
                                const float* k_scale, int64_t pool_pages, const int32_t* block_table_host,
                                int n_req, int max_pages, const int32_t* seq_lens_host,
@@ -321,9 +432,19 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
         return IDX_ERR_ARG;
     if (!workspace) return IDX_ERR_WORKSPACE;
     if (!aligned(workspace, 1024)) return IDX_ERR_ALIGN;
-    const HostLayout H = host_layout(R, max_len, k, n_req, max_pages);
-    if (ws_bytes < H.end) return IDX_ERR_WORKSPACE;
-    char* ws = static_cast<char*>(workspace);
+    HostCall c{};
+    c.qtype = qtype;
+    c.R = R;
+    c.max_pages = max_pages;
+    c.k = k;
+    c.k_cache = k_cache;
+    c.k_scale = k_scale;
+    c.pool_pages = pool_pages;
+    c.max_len = max_len;
+    c.ws = static_cast<char*>(workspace);
+    c.ws_bytes = ws_bytes;
+    c.H = host_layout(R, max_len, k, n_req, max_pages);
+    if (ws_bytes < c.H.end) return IDX_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Inputs in page-locked, mapped host memory are gathered by one kernel that
     // reads them over the host link; any other buffer is copied by the copy engine.
@@ -331,43 +452,40 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
         const void* host;
         size_t off, bytes;
     } in[kStageMaxCopies] = {
-        {q_host, H.q, (size_t)R * kHeads * kDim * (qtype == IDX_Q_E4M3 ? 1 : 2)},
-        {head_w_host, H.w, (size_t)R * kHeads * 4},
-        {block_table_host, H.bt, (size_t)n_req * (size_t)max_pages * 4},
-        {seq_lens_host, H.lens, (size_t)R * 4},
-        {row_req_host, H.rreq, (size_t)R * 4},
+        {q_host, c.H.q, (size_t)R * kHeads * kDim * (qtype == IDX_Q_E4M3 ? 1 : 2)},
+        {head_w_host, c.H.w, (size_t)R * kHeads * 4},
+        {block_table_host, c.H.bt, (size_t)n_req * (size_t)max_pages * 4},
+        {seq_lens_host, c.H.lens, (size_t)R * 4},
+        {row_req_host, c.H.rreq, (size_t)R * 4},
     };
-    StagePlan plan{};
     for (const auto& b : in) {
         const void* d = mapped(b.host);
         if (d && aligned(d, 16) && b.bytes % 4 == 0 && b.bytes < (1ull << 31)) {
-            plan.c[plan.n++] = StageCopy{d, ws + b.off, (uint32_t)b.bytes};
-        } else if (cudaMemcpyAsync(ws + b.off, b.host, b.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return IDX_ERR_CUDA;
+            c.plan.c[c.plan.n++] = StageCopy{d, c.ws + b.off, (uint32_t)b.bytes};
+        } else {
+            c.copy[c.n_copy].host = b.host;
+            c.copy[c.n_copy].off = b.off;
+            c.copy[c.n_copy].bytes = b.bytes;
+            ++c.n_copy;
         }
     }
-    if (plan.n > 0 && launch_stage(plan, s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return IDX_ERR_CUDA;
-    }
     // The selection writes the indices straight into mapped host memory.
-    int32_t* idx_dev = reinterpret_cast<int32_t*>(ws + H.idx);
-    int32_t* idx_out = idx_dev;
+    c.indices_host = indices_host;
+    c.idx_out = reinterpret_cast<int32_t*>(c.ws + c.H.idx);
     const void* out_map = mapped(indices_host);
-    if (out_map && aligned(out_map, 4)) idx_out = const_cast<int32_t*>(static_cast<const int32_t*>(out_map));
-    const idx_status st = idx_score_topk(qtype, ws + H.q, reinterpret_cast<const float*>(ws + H.w), k_cache, k_scale,
-                                         pool_pages, reinterpret_cast<const int32_t*>(ws + H.bt), max_pages,
-                                         reinterpret_cast<const int32_t*>(ws + H.lens),
-                                         reinterpret_cast<const int32_t*>(ws + H.rreq), R, max_len, k, idx_out,
-                                         nullptr, 0, workspace, ws_bytes, stream);
-    if (st != IDX_OK) return st;
-    if (idx_out == idx_dev &&
-        cudaMemcpyAsync(indices_host, idx_dev, (size_t)R * (size_t)k * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return IDX_ERR_CUDA;
-    }
-    return IDX_OK;
+    if (out_map && aligned(out_map, 4)) c.idx_out = const_cast<int32_t*>(static_cast<const int32_t*>(out_map));
+    // One graph when every buffer is mapped (no pageable copy, which a graph
+    // cannot hold) and the stream is an explicit one that is not capturing
+    // already (a caller's capture takes the launches as they are).
+    const bool all_mapped = c.n_copy == 0 && c.idx_out != reinterpret_cast<int32_t*>(c.ws + c.H.idx);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusActive;
+    int dev = 0;
+    if (all_mapped && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread &&
+        cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
+        cudaGetDevice(&dev) == cudaSuccess)
+        return host_launches_graph(c, s, dev);
+    (void)cudaGetLastError();
+    return host_launches(c, s);
 }
 
 idx_status idx_check_status(void* workspace, void* stream) {

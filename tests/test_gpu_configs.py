@@ -117,6 +117,36 @@ def test_host_buffer_call_matches_device_call(cfg, pinned):
     assert np.array_equal(out.numpy(), ref)
 
 
+def test_host_buffer_calls_on_a_stream():
+    """On an explicit stream with every buffer page-locked, idx_score_topk_host
+    runs each call as this thread's cached CUDA graph (updated per call): five
+    calls issued back to back with no synchronisation, alternating workloads
+    of different shapes and inputs, each into its own host indices, all give
+    the device call's lists."""
+    loads = [W.make_config(4), W.make_config(2), W.make_config(4, seed=44), W.make_config(1), W.make_config(4)]
+    refs, args = [], []
+    for w in loads:
+        t = device_inputs(w)
+        _, ref, st = gpu_fused(w, t)
+        assert st == 0
+        refs.append(ref)
+        pin = lambda x: x.contiguous().pin_memory()
+        ws = binding.new_host_workspace(w.R, w.max_len, w.k, w.block_table.shape[0], w.block_table.shape[1])
+        out = pin(torch.full((w.R, w.k), -7, dtype=torch.int32))
+        args.append((pin(w.q), pin(w.head_w), t["k_cache"], t["k_scale"], pin(w.block_table), pin(w.seq_lens),
+                     pin(w.row_req), w.max_len, w.k, out, ws))
+    stream = torch.cuda.Stream()
+    binding.score_topk_host(*args[0], stream=stream)  # the thread's first call on this path runs eagerly
+    stream.synchronize()
+    args[0][9].fill_(-7)
+    for a in args:
+        binding.score_topk_host(*a, stream=stream)
+    stream.synchronize()
+    for a, ref in zip(args, refs):
+        assert binding.check_status(a[10], stream) == 0
+        assert np.array_equal(a[9].numpy(), ref)
+
+
 @pytest.mark.parametrize("cfg", [2, 4])
 def test_slot_lists(cfg):
     """idx_score_topk_slots: the same lists as idx_score_topk, each position
