@@ -28,12 +28,17 @@
 //    barrier each thread reads its four bins' totals from their owner with
 //    one 16-byte remote load, then the block scans them.  No slice spins on
 //    another; every wait is a cluster barrier.
-//  * Each thread then owns a contiguous run of the slice's positions: one
-//    block scan of its packed (above T, at T) counts gives its offsets within
-//    the slice, each slice stores its totals into every later slice, and
-//    after one more barrier the positions are written in order: keys above T
-//    first, then ties, each in ascending position (or, for the slot variant,
-//    the cache slots those positions map to).
+//  * In the last round each thread scans its own contiguous run of the
+//    slice's positions, counting its keys above the 22-bit prefix and marking
+//    those that match it; each slice sends its count above the prefix and its
+//    non-zero last-digit bins (at most 8 of them) to the other slices with the
+//    round's histogram, so after that round's barrier every slice knows how
+//    many keys above T and at T the slices before it hold.  Only when some
+//    slice has more non-zero bins does one more exchange (and barrier) follow.
+//    One block scan of the threads' packed (above T, at T) counts gives their
+//    offsets, and the positions are written in order: keys above T first,
+//    then ties, each in ascending position (or, for the slot variant, the
+//    cache slots those positions map to).
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -49,7 +54,9 @@ constexpr int kBinsMax = 2048;
 constexpr int kSliceTarget = 4096;  // keys per slice the launcher aims for
 constexpr int kSliceCapMax = 32768; // keys one slice can hold (128 KB of shared memory)
 constexpr int kMaxCluster = 16;
+constexpr uint32_t kMail = 8;  // last-digit bins a slice sends to the later slices
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+static_assert(kSliceCapMax / kThreads <= 32, "a thread's keys fit one 32-bit mask");
 
 // ---------------------------------------------------------------- cluster PTX
 
@@ -95,6 +102,11 @@ struct __align__(16) Shared {
     uint32_t hloc[kBinsMax];             // this slice's histogram of the round
     uint32_t htot[3][kBinsMax];          // totals of every slice, one buffer per round
     uint32_t cnt[2][kMaxCluster];        // counts above / at T of every earlier slice
+    uint32_t mail[kMaxCluster][kMail];   // last round: slice t's non-zero bins, (bin << 16) | count
+    uint32_t mail_n[kMaxCluster];        // last round: slice t's non-zero bins (> kMail: not all sent)
+    uint32_t mail_above[kMaxCluster];    // last round: slice t's keys above the prefix
+    uint32_t nz, above;                  // this slice's non-zero last-round bins, keys above the prefix
+    uint32_t base[3];                    // keys above / at T before this slice; 1 if a slice sent too many bins
     uint32_t wsum[kWarps];
     uint32_t pick[3];                    // digit, keys above it, keys in it
 };
@@ -128,12 +140,50 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, Shar
 // whose bits above the digit equal `prefix` under `mask` (or over S.hloc as
 // built by the caller, when `have_hist`).  Leaves the digit holding rank kr
 // (counted from the largest digit), the number of keys above it and the
-// number in it in S.pick.  One copy of this code serves all rounds.
+// number in it in S.pick.
+//
+// The `last` round also prepares the ordered writes: each thread scans its
+// own run of positions [4 j0, 4 j1) and leaves its keys above the prefix in
+// *above and, in *cmask, which of its keys match the prefix (bit 4 (j - j0)
+// + q for position 4 j + q); the slice's count above the prefix and its
+// non-zero bins (up to kMail of them, with their counts) go to the other
+// slices ahead of the round's cluster barrier.
 __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, int cnt, uint32_t prefix,
                                          uint32_t mask, int shift, int nb, uint32_t kr, bool single, int r,
-                                         int nslices, bool have_hist, Shared& S) {
+                                         int nslices, bool have_hist, Shared& S, bool last = false,
+                                         uint32_t c = 0, int j0 = 0, int j1 = 0, uint32_t* above_out = nullptr,
+                                         uint32_t* cmask_out = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (!have_hist) {
+    if (!have_hist && last) {
+        for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
+        if (tid == 0) {
+            S.nz = 0;
+            S.above = 0;
+        }
+        __syncthreads();
+        const uint32_t dm = (uint32_t)nb - 1;
+        uint32_t above = 0, cm = 0;
+        for (int j = j0; j < j1; ++j) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys)[j];
+            const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (4 * j + q < cnt) {
+                    const uint32_t hi = uu[q] & mask;
+                    if (hi == prefix) {
+                        atomicAdd(&S.hloc[(uu[q] >> shift) & dm], 1u);
+                        cm |= 1u << (4 * (j - j0) + q);
+                    } else {
+                        above += (uint32_t)(hi > prefix);
+                    }
+                }
+            }
+        }
+        *above_out = above;
+        *cmask_out = cm;
+        above = __reduce_add_sync(kFull, above);
+        if (lane == 0 && above) atomicAdd(&S.above, above);
+    } else if (!have_hist) {
         for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
         __syncthreads();
         const uint32_t dm = (uint32_t)nb - 1;
@@ -178,7 +228,22 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
         const int per_owner = nb / nslices;
         for (int b = tid; b < nb; b += kThreads) {
             const uint32_t v = S.hloc[b];
-            if (v) red_add_remote(map_rank(&S.htot[r][b], (uint32_t)(b / per_owner)), v);
+            if (v) {
+                red_add_remote(map_rank(&S.htot[r][b], (uint32_t)(b / per_owner)), v);
+                if (last) {
+                    const uint32_t slot = atomicAdd(&S.nz, 1u);
+                    if (slot < kMail)
+                        for (int t = (int)c + 1; t < nslices; ++t)
+                            st_remote(map_rank(&S.mail[c][slot], (uint32_t)t), ((uint32_t)b << 16) | v);
+                }
+            }
+        }
+        if (last) {
+            __syncthreads();  // S.nz and S.above are final
+            if (tid < nslices && tid != (int)c) {
+                st_remote(map_rank(&S.mail_n[c], (uint32_t)tid), S.nz);
+                st_remote(map_rank(&S.mail_above[c], (uint32_t)tid), S.above);
+            }
         }
         cluster_arrive();
         cluster_wait();
@@ -340,40 +405,72 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     __syncthreads();
     if (!single) cluster_wait();
 
-    // ---- digit rounds: bits 31..21, then 20..10 and 9..0 ----------------------
-    uint32_t prefix = 0, mask = 0, kr = (uint32_t)k;
-#pragma unroll 1
-    for (int r = 0; r < 3; ++r) {
-        const int shift = r == 0 ? 21 : (r == 1 ? 10 : 0);
-        const int nb = r == 2 ? 1024 : 2048;
-        digit_round(keys_s, cnt, prefix, mask, shift, nb, kr, single, r, CL, r == 0, S);
-        prefix |= S.pick[0] << shift;
-        mask |= (uint32_t)(nb - 1) << shift;
-        kr -= S.pick[1];
-    }
-    const uint32_t T = prefix;            // the k-th largest radix key of the row
-    const uint32_t gt_total = (uint32_t)k - kr;
-
-    // ---- thread tid owns the slice's positions [4 j0, 4 j1): its counts above
-    //      and at T, packed (above < 2^11, at <= slice_cap < 2^16), scanned in
-    //      thread order ------------------------------------------------------------
+    // ---- digit rounds: bits 31..21, then 20..10 and 9..0; thread tid owns the
+    //      slice's positions [4 j0, 4 j1) in the last round and the writes -------
     const int n4 = (cnt + 3) >> 2;
     const int m4 = (n4 + kThreads - 1) / kThreads;
     const int j0 = tid * m4 < n4 ? tid * m4 : n4;
     const int j1 = j0 + m4 < n4 ? j0 + m4 : n4;
-    uint32_t mine = 0;
-    for (int j = j0; j < j1; ++j) {
-        const uint4 u = reinterpret_cast<const uint4*>(keys_s)[j];
-        const int i = 4 * j;
-        mine += ((uint32_t)(i + 0 < cnt && u.x > T) << 16) + (uint32_t)(i + 0 < cnt && u.x == T);
-        mine += ((uint32_t)(i + 1 < cnt && u.y > T) << 16) + (uint32_t)(i + 1 < cnt && u.y == T);
-        mine += ((uint32_t)(i + 2 < cnt && u.z > T) << 16) + (uint32_t)(i + 2 < cnt && u.z == T);
-        mine += ((uint32_t)(i + 3 < cnt && u.w > T) << 16) + (uint32_t)(i + 3 < cnt && u.w == T);
+    uint32_t prefix = 0, mask = 0, kr = (uint32_t)k;
+#pragma unroll 1
+    for (int r = 0; r < 2; ++r) {
+        const int shift = r == 0 ? 21 : 10;
+        digit_round(keys_s, cnt, prefix, mask, shift, 2048, kr, single, r, CL, r == 0, S);
+        prefix |= S.pick[0] << shift;
+        mask |= 0x7FFu << shift;
+        kr -= S.pick[1];
+    }
+    uint32_t above = 0, cmask = 0;
+    digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, false, S, true, c, j0, j1, &above, &cmask);
+    const uint32_t d_last = S.pick[0];
+    const uint32_t T = prefix | d_last;   // the k-th largest radix key of the row
+    kr -= S.pick[1];
+    const uint32_t gt_total = (uint32_t)k - kr;
+
+    // ---- this thread's counts above and at T, packed (above < 2^11, at <=
+    //      slice_cap < 2^16), scanned in thread order; only the keys that match
+    //      the prefix are looked at again --------------------------------------
+    uint32_t gt = above, eq = 0;
+    for (uint32_t m = cmask; m; m &= m - 1) {
+        const uint32_t u = keys_s[4 * j0 + (__ffs(m) - 1)];
+        gt += (uint32_t)(u > T);
+        eq += (uint32_t)(u == T);
+    }
+    const uint32_t mine = (gt << 16) | eq;
+    if (!single && (tid >> 5) == 0) {
+        // Keys above / at T in the slices before this one, from what they sent
+        // with the last round (lane t: slice t), unless a slice had more
+        // non-zero bins than it could send.
+        const int lane = tid & 31;
+        uint32_t n_t = 0, g_t = 0, e_t = 0;
+        if (lane < CL) {
+            n_t = lane == (int)c ? S.nz : S.mail_n[lane];
+            if (lane < (int)c) {
+                g_t = S.mail_above[lane];
+                const uint32_t ne = n_t < kMail ? n_t : kMail;
+                for (uint32_t e = 0; e < ne; ++e) {
+                    const uint32_t x = S.mail[lane][e];
+                    if ((x >> 16) > d_last) g_t += x & 0xFFFFu;
+                    else if ((x >> 16) == d_last) e_t += x & 0xFFFFu;
+                }
+            }
+        }
+        const uint32_t ovf = __any_sync(kFull, n_t > kMail) ? 1u : 0u;
+        g_t = __reduce_add_sync(kFull, g_t);
+        e_t = __reduce_add_sync(kFull, e_t);
+        if (lane == 0) {
+            S.base[0] = g_t;
+            S.base[1] = e_t;
+            S.base[2] = ovf;
+        }
     }
     uint32_t total;
-    const uint32_t off = block_scan(mine, &total, S);
+    const uint32_t off = block_scan(mine, &total, S);  // its barriers also publish S.base
     uint32_t base_gt = 0, base_eq = 0;
-    if (!single) {
+    if (!single && !S.base[2]) {
+        base_gt = S.base[0];
+        base_eq = S.base[1];
+    } else if (!single) {
         // this slice's counts into every later slice (kept apart: a row's ties
         // may outnumber 2^16)
         if (tid > (int)c && tid < CL) {

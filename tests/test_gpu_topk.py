@@ -198,3 +198,22 @@ def test_crowded_first_digit(n, placement, c1):
     got, st = gpu_topk(s[None, :], [n], 2048)
     assert st == 0
     _check_rows(s[None, :], [n], 2048, got)
+
+
+@pytest.mark.parametrize("n", [30000, 131072])
+@pytest.mark.parametrize("distinct", [1, 3, 8, 9, 40, 1024])
+def test_last_digit_bins(n, distinct):
+    """The k-th key shares its top 22 bits with 3,000 keys spread over the
+    row, whose last 10 bits take `distinct` values: a slice with at most 8
+    non-zero last-digit bins sends them with the last round, one with more
+    makes every slice exchange its counts once more."""
+    rng = np.random.default_rng(n + distinct)
+    s = rng.uniform(0.1, 0.9, n).astype(np.float32)
+    pos = rng.choice(n, 4000, replace=False)
+    s[pos[:1000]] = rng.uniform(2.0, 4.0, 1000).astype(np.float32)
+    low = rng.choice(1024, distinct, replace=False)
+    bits = np.uint32(0x3F800000) + low[rng.integers(0, distinct, 3000)].astype(np.uint32)
+    s[pos[1000:]] = bits.view(np.float32)          # 1.0 + low / 2^23: one 22-bit prefix
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
