@@ -52,6 +52,7 @@ static_assert(kThreads >= 256 && kThreads <= 1024 && kThreads % 256 == 0, "block
 constexpr int kLoadUnroll = 4096 / kThreads;  // float4 reads in flight per thread (16K keys a CTA)
 constexpr int kBinsMax = 2048;
 constexpr int kSliceTarget = 4096;  // keys per slice the launcher aims for
+constexpr int kSingleMax = 12288;   // rows up to this long run on one CTA each (no cluster barrier)
 constexpr int kSliceCapMax = 32768; // keys one slice can hold (128 KB of shared memory)
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kMail = 8;  // last-digit bins a slice sends to the later slices
@@ -606,13 +607,17 @@ int max_active_clusters(int cap) {
 
 int64_t select_max_len(int cluster) { return (int64_t)cluster * kSliceCapMax; }
 
-// The cluster size: the largest of 16, 8, 4, 2, 1 CTAs, but no more than the
-// longest row's slices of kSliceTarget keys, whose slices hold the longest
-// row and whose clusters for all rows are resident at once; when no
-// size fits the rows in one wave, the smallest size that holds the row (the
-// most rows at once).  A row's slices then do more work each, but every CTA's
-// time is mostly fixed latencies (barriers, exchanges), so fewer waves win.
+// The cluster size: one CTA per row when the longest row has at most
+// kSingleMax keys (its three passes over the keys cost less than the cluster
+// barriers of a split row); otherwise the largest of 16, 8, 4, 2, 1 CTAs, but
+// no more than the longest row's slices of kSliceTarget keys, whose slices
+// hold the longest row and whose clusters for all rows are resident at once;
+// when no size fits the rows in one wave, the smallest size that holds the
+// row (the most rows at once).  A row's slices then do more work each, but
+// every CTA's time is mostly fixed latencies (barriers, exchanges), so fewer
+// waves win.
 cudaError_t launch_select(const SelectArgs& a) {
+    if (a.max_len <= kSingleMax && max_active_clusters<1>(slice_cap_for(1, a.max_len)) > 0) return launch_c<1>(a);
     int chosen = 0;
     const int sizes[] = {16, 8, 4, 2, 1};
     // no more CTAs than the longest row has slices of kSliceTarget keys: extra

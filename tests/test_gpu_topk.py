@@ -217,3 +217,16 @@ def test_last_digit_bins(n, distinct):
     got, st = gpu_topk(s[None, :], [n], 2048)
     assert st == 0
     _check_rows(s[None, :], [n], 2048, got)
+
+
+@pytest.mark.parametrize("R,n", [(64, 20000), (200, 13000), (6, 12288), (6, 12289)])
+def test_row_count_and_length_mixes(R, n):
+    """Launches whose rows the launcher places on one CTA each (up to 12,288
+    keys), on clusters of 2 (64 rows of 20,000 keys: larger clusters would
+    not all be resident) or on one CTA each again (200 rows)."""
+    rng = np.random.default_rng(R * n)
+    s = rng.standard_normal((R, n)).astype(np.float32)
+    lens = [n - (r % 3) for r in range(R)]
+    got, st = gpu_topk(s, lens, 2048)
+    assert st == 0
+    _check_rows(s, lens, 2048, got)
