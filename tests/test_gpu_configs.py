@@ -147,6 +147,38 @@ def test_host_buffer_calls_on_a_stream():
         assert np.array_equal(a[9].numpy(), ref)
 
 
+def test_host_buffer_call_error_inside_its_graph():
+    """An argument error found while the host-buffer call captures its launches
+    (a key cache that is not 16-byte aligned) is returned, ends the capture,
+    and leaves the stream and the thread's graph usable: the next call gives
+    the device call's lists."""
+    w = W.make_config(1)
+    t = device_inputs(w)
+    _, ref, st = gpu_fused(w, t)
+    assert st == 0
+    pin = lambda x: x.contiguous().pin_memory()
+    q, hw, bt, sl, rq = pin(w.q), pin(w.head_w), pin(w.block_table), pin(w.seq_lens), pin(w.row_req)
+    out = pin(torch.full((w.R, w.k), -7, dtype=torch.int32))
+    ws = binding.new_host_workspace(w.R, w.max_len, w.k, w.block_table.shape[0], w.block_table.shape[1])
+    stream = torch.cuda.Stream()
+    lib = binding.load()
+
+    def call(kc_offset):
+        return lib.idx_score_topk_host(0, q.data_ptr(), hw.data_ptr(), t["k_cache"].data_ptr() + kc_offset,
+                                       t["k_scale"].data_ptr(), t["k_cache"].shape[0], bt.data_ptr(),
+                                       bt.shape[0], bt.shape[1], sl.data_ptr(), rq.data_ptr(), w.R, w.max_len,
+                                       w.k, out.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    assert call(0) == 0 and call(0) == 0  # a direct call, then one through the thread's graph
+    assert call(1) == -2                   # IDX_ERR_ALIGN, raised inside the capture
+    with torch.cuda.stream(stream):
+        assert not torch.cuda.is_current_stream_capturing()
+    out.fill_(-7)
+    assert call(0) == 0
+    stream.synchronize()
+    assert binding.check_status(ws, stream) == 0
+    assert np.array_equal(out.numpy(), ref)
+
+
 @pytest.mark.parametrize("cfg", [2, 4])
 def test_slot_lists(cfg):
     """idx_score_topk_slots: the same lists as idx_score_topk, each position
