@@ -68,6 +68,7 @@ constexpr uint32_t kPageScaleBytes = kPage * 4;            // 256 B
 constexpr uint32_t kStageBytes = kTileKeys * kDim;         // 16 KB
 constexpr uint32_t kStageScaleBytes = kTileKeys * 4;       // 512 B
 constexpr uint32_t kAccCols = 256;
+constexpr int kRegWTilesPerCta = 32;  // launches of at least this many tiles per CTA keep weights in registers
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 
 constexpr uint32_t kOffQHi = 0;
@@ -331,6 +332,12 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
+// kRegW: the epilogue keeps the first 32 head weights of its row in registers
+// for a group's tiles and reads the TMEM accumulator 16 columns at a time
+// (room for them under the register cap of 18 warps); the weights' broadcast
+// shared-memory reads otherwise share the shared-memory pipe with the tensor
+// core's operand reads in every tile.  It pays when a CTA has many tiles.
+template <bool kRegW>
 __global__ void __launch_bounds__(kScoreThreads, 1)
 k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -496,6 +503,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         int g = find_group(pl, n_groups, it0), li = 0, qi = 0;
         int gend = -1, gbeg = 0, r0 = 0, nr = 0, rlen = 0;
         const float* w = wq_s;
+        uint64_t wr[kRegW ? 16 : 1];  // kRegW: w' of heads 0..31 of this warp's row, packed pairs
         for (int it = it0; it < it1; ++it, ++li) {
             if (it >= gend) {
                 // A new group.  Every MMA that read the previous group's query has
@@ -514,6 +522,14 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 if (lane == 0) mbar_arrive(qfull);
                 if (!bounded_wait(qfull, qi & 1, abort_flag)) break;  // every warp's w' is written
                 w = wbuf + rr * kHeads;
+                if constexpr (kRegW) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 x = *reinterpret_cast<const float4*>(w + 4 * j);
+                        wr[2 * j] = pack2(x.x, x.y);
+                        wr[2 * j + 1] = pack2(x.z, x.w);
+                    }
+                }
                 ++qi;
             }
             const int s = li % kStages, acc = li & 1;
@@ -531,25 +547,61 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                        (uint32_t)acc * kAccCols + (uint32_t)rr * kHeads;
                 uint64_t a[4] = {0ull, 0ull, 0ull, 0ull};  // four packed (2 x f32) partial sums
+                // Heads in the same order either way: a[j] takes head pairs
+                // (8 i + 2 j, 8 i + 2 j + 1) for i = 0 .. 7.
+                if constexpr (kRegW) {
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float v[32];
-                    tmem_load_32cols(taddr + 32 * hf, v);
-                    if (hf == 1) {
-                        // every column of this warp is in registers: release the
-                        // accumulator before the second half's arithmetic
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                    for (int ch = 0; ch < 4; ++ch) {  // 16 head columns at a time
+                        float v[16];
+                        tmem_load_16cols(taddr + 16 * ch, v);
+                        if (ch == 3) {
+                            // every column of this warp is in registers: release
+                            // the accumulator before the last chunk's arithmetic
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[acc]);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 16; h += 8) {
+                            uint64_t wp[4];
+                            if (ch < 2) {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) wp[j] = wr[(16 * ch + h) / 2 + j];
+                            } else {
+                                const float4 w0 = *reinterpret_cast<const float4*>(w + 16 * ch + h);
+                                const float4 w1 = *reinterpret_cast<const float4*>(w + 16 * ch + h + 4);
+                                wp[0] = pack2(w0.x, w0.y);
+                                wp[1] = pack2(w0.z, w0.w);
+                                wp[2] = pack2(w1.x, w1.y);
+                                wp[3] = pack2(w1.z, w1.w);
+                            }
+                            a[0] = ffma2(wp[0], pack2(relu2(v[h + 0]), relu2(v[h + 1])), a[0]);
+                            a[1] = ffma2(wp[1], pack2(relu2(v[h + 2]), relu2(v[h + 3])), a[1]);
+                            a[2] = ffma2(wp[2], pack2(relu2(v[h + 4]), relu2(v[h + 5])), a[2]);
+                            a[3] = ffma2(wp[3], pack2(relu2(v[h + 6]), relu2(v[h + 7])), a[3]);
+                        }
                     }
+                } else {
 #pragma unroll
-                    for (int h = 0; h < 32; h += 8) {
-                        const float4 w0 = *reinterpret_cast<const float4*>(w + 32 * hf + h);
-                        const float4 w1 = *reinterpret_cast<const float4*>(w + 32 * hf + h + 4);
-                        a[0] = ffma2(pack2(w0.x, w0.y), pack2(relu2(v[h + 0]), relu2(v[h + 1])), a[0]);
-                        a[1] = ffma2(pack2(w0.z, w0.w), pack2(relu2(v[h + 2]), relu2(v[h + 3])), a[1]);
-                        a[2] = ffma2(pack2(w1.x, w1.y), pack2(relu2(v[h + 4]), relu2(v[h + 5])), a[2]);
-                        a[3] = ffma2(pack2(w1.z, w1.w), pack2(relu2(v[h + 6]), relu2(v[h + 7])), a[3]);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float v[32];
+                        tmem_load_32cols(taddr + 32 * hf, v);
+                        if (hf == 1) {
+                            // every column of this warp is in registers: release the
+                            // accumulator before the second half's arithmetic
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[acc]);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 32; h += 8) {
+                            const float4 w0 = *reinterpret_cast<const float4*>(w + 32 * hf + h);
+                            const float4 w1 = *reinterpret_cast<const float4*>(w + 32 * hf + h + 4);
+                            a[0] = ffma2(pack2(w0.x, w0.y), pack2(relu2(v[h + 0]), relu2(v[h + 1])), a[0]);
+                            a[1] = ffma2(pack2(w0.z, w0.w), pack2(relu2(v[h + 2]), relu2(v[h + 3])), a[1]);
+                            a[2] = ffma2(pack2(w1.x, w1.y), pack2(relu2(v[h + 4]), relu2(v[h + 5])), a[2]);
+                            a[3] = ffma2(pack2(w1.z, w1.w), pack2(relu2(v[h + 6]), relu2(v[h + 7])), a[3]);
+                        }
                     }
                 }
                 const float2 s0 = unpack2(a[0]), s1 = unpack2(a[1]), s2 = unpack2(a[2]), s3 = unpack2(a[3]);
@@ -582,7 +634,9 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        err = cudaFuncSetAttribute(k_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        err = cudaFuncSetAttribute(k_score<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(k_score<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         configured_device = dev;
     }
@@ -601,7 +655,13 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.scores = a.scores;
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
-    k_score<<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
+    // Tiles per CTA, at least (the rows form at least ceil(R / 4) groups, each
+    // of up to len_cap keys): the register-held weights from 32 on.
+    const int64_t tiles = (int64_t)((a.R + kGroupRows - 1) / kGroupRows) * ((p.len_cap + kTileKeys - 1) / kTileKeys);
+    if (tiles >= (int64_t)kRegWTilesPerCta * a.num_sms)
+        k_score<true><<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
+    else
+        k_score<false><<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
     return cudaGetLastError();
 }
 
