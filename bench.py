@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-8k", action="store_true")
     ap.add_argument("--no-fp8q", action="store_true", help="skip the FP8-query measurement")
     ap.add_argument("--no-batch", action="store_true", help="skip the 64-row measurement")
+    ap.add_argument("--no-warm", action="store_true", help="skip the L2-resident measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     return ap.parse_args()
 
@@ -473,6 +474,17 @@ def main():
         line["also_8k"] = {"workload": w8.recipe, "us": sec8 * 1e6,
                            "keys_per_s": w8.row_keys() / sec8}
         del st8
+    if not args.no_warm:
+        # the same workload with a single key-cache copy, which stays in L2
+        # between steps (the figure beside the rotated, HBM-bound one)
+        stw = Step(w, 1, dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                stw.fused(i, stream)
+            secw = time_graph_steps(stw, min(args.steps, 4096), stream, None)
+        line["also_warm_l2"] = {"workload": w.recipe + "; one key-cache copy, resident in L2 between steps",
+                                "us": secw * 1e6, "keys_per_s": w.row_keys() / secw}
+        del stw
     if not args.no_batch:
         # batch context: 16 requests x 4 verify rows (64 rows, 277 MB of keys)
         wb = W.make_config(5)
