@@ -388,6 +388,9 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // Launched as a programmatic dependent (after the host call's stage
+    // kernel): wait for that grid before reading any input.  A no-op otherwise.
+    pdl_wait();
     if (warp == 0) build_plan(p, pl, &counts[0], &counts[1]);
     tc_fence_before_sync();
     __syncthreads();
@@ -658,11 +661,21 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     // Tiles per CTA, at least (the rows form at least ceil(R / 4) groups, each
     // of up to len_cap keys): the register-held weights from 32 on.
     const int64_t tiles = (int64_t)((a.R + kGroupRows - 1) / kGroupRows) * ((p.len_cap + kTileKeys - 1) / kTileKeys);
-    if (tiles >= (int64_t)kRegWTilesPerCta * a.num_sms)
-        k_score<true><<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
-    else
-        k_score<false><<<a.num_sms, kScoreThreads, kSmemBytes, a.stream>>>(keys_map, p);
-    return cudaGetLastError();
+    const bool reg_w = tiles >= (int64_t)kRegWTilesPerCta * a.num_sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.num_sms, 1, 1);
+    cfg.blockDim = dim3(kScoreThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    if (a.after_stage) {  // may begin while the stage kernel before it runs
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return reg_w ? cudaLaunchKernelEx(&cfg, k_score<true>, keys_map, p)
+                 : cudaLaunchKernelEx(&cfg, k_score<false>, keys_map, p);
 }
 
 }  // namespace idx

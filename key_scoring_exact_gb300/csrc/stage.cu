@@ -4,6 +4,7 @@
 // whose threads read the buffers directly replaces one copy-engine transfer
 // (several microseconds of fixed cost each) per buffer.
 #include "idx_internal.h"
+#include "ptx.cuh"
 
 namespace idx {
 
@@ -12,6 +13,7 @@ namespace {
 constexpr int kStageThreads = 256;
 
 __global__ void __launch_bounds__(kStageThreads) k_stage(StagePlan plan) {
+    pdl_launch_dependents();  // the scoring kernel may launch now; it waits for this grid's end
     const StageCopy cp = plan.c[blockIdx.y];
     const uint32_t n16 = cp.bytes / 16, n4 = cp.bytes / 4;
     const uint32_t stride = gridDim.x * kStageThreads;
