@@ -185,7 +185,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                           const float* k_scale, int64_t pool_pages, const int32_t* block_table, int max_pages,
                           const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
-                          size_t ws_bytes, void* stream, bool slots, bool after_stage = false) {
+                          size_t ws_bytes, void* stream, bool slots) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
@@ -209,7 +209,6 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                 R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
-    a.after_stage = after_stage;
     st = run_score(a);
     if (st != IDX_OK) return st;
     // Each row's selection covers the keys its scores were written for.
@@ -346,14 +345,14 @@ idx_status host_launches(const HostCall& c, cudaStream_t s) {
         return IDX_ERR_CUDA;
     }
     const HostLayout& H = c.H;
-    // The scoring kernel is a programmatic dependent of the stage kernel: its
-    // CTAs launch and set up while the stage runs, and wait for it to finish
-    // before reading what it wrote.
-    const idx_status st = score_topk_impl(
-        c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale, c.pool_pages,
-        reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages, reinterpret_cast<const int32_t*>(c.ws + H.lens),
-        reinterpret_cast<const int32_t*>(c.ws + H.rreq), c.R, c.max_len, c.k, c.idx_out, nullptr, 0, c.ws,
-        c.ws_bytes, s, false, c.plan.n > 0 && c.n_copy == 0);
+    // (The scoring kernel launches as a programmatic dependent of the stage
+    // kernel: its CTAs set up while the stage runs and wait for it to finish
+    // before reading what it wrote.)
+    const idx_status st =
+        idx_score_topk(c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale,
+                       c.pool_pages, reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages,
+                       reinterpret_cast<const int32_t*>(c.ws + H.lens), reinterpret_cast<const int32_t*>(c.ws + H.rreq),
+                       c.R, c.max_len, c.k, c.idx_out, nullptr, 0, c.ws, c.ws_bytes, s);
     if (st != IDX_OK) return st;
     int32_t* idx_dev = reinterpret_cast<int32_t*>(c.ws + H.idx);
     if (c.idx_out == idx_dev && cudaMemcpyAsync(c.indices_host, idx_dev, (size_t)c.R * (size_t)c.k * 4,

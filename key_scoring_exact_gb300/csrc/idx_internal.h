@@ -65,7 +65,6 @@ struct ScoreArgs {
     WsLayout L;
     cudaStream_t stream;
     int num_sms;
-    bool after_stage = false;  // launched as a programmatic dependent of the stage kernel before it
 };
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);

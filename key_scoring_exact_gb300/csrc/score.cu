@@ -388,8 +388,9 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // Launched as a programmatic dependent (after the host call's stage
-    // kernel): wait for that grid before reading any input.  A no-op otherwise.
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: wait for that grid to finish before reading an input or writing
+    // a score (only barriers and TMEM are set up before this point).
     pdl_wait();
     if (warp == 0) build_plan(p, pl, &counts[0], &counts[1]);
     tc_fence_before_sync();
@@ -667,13 +668,16 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     cfg.blockDim = dim3(kScoreThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = a.stream;
+    // A programmatic dependent of the kernel before it on the stream: its CTAs
+    // may launch (on SMs that kernel leaves free) once that kernel allows it,
+    // and wait for it to finish (griddepcontrol.wait) before touching global
+    // memory.  The selection allows it at its start, the host call's gather
+    // kernel too; any other kernel before it simply completes first.
     cudaLaunchAttribute attr[1];
-    if (a.after_stage) {  // may begin while the stage kernel before it runs
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return reg_w ? cudaLaunchKernelEx(&cfg, k_score<true>, keys_map, p)
                  : cudaLaunchKernelEx(&cfg, k_score<false>, keys_map, p);
 }

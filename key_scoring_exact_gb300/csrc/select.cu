@@ -322,6 +322,10 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     const uint32_t c = cluster_ctarank();
     const int row = blockIdx.y;
     const int tid = threadIdx.x;
+    // The next launch on the stream (the next step's scoring) may start setting
+    // up on the SMs this launch leaves free; it waits for this grid to finish
+    // before it reads or writes anything in global memory.
+    pdl_launch_dependents();
 
     // Slice c covers positions [c * slice_cap, (c + 1) * slice_cap) of the row
     // (slice_cap is fixed by the launch's length bound), so its score loads
