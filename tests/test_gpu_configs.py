@@ -147,6 +147,37 @@ def test_host_buffer_calls_on_a_stream():
         assert np.array_equal(a[9].numpy(), ref)
 
 
+def test_back_to_back_calls_share_a_workspace():
+    """Fused device calls issued back to back on one stream with no
+    synchronisation, alternating two workloads, all with the scores in one
+    shared workspace: each scoring launch may start while the previous
+    selection runs (a programmatic dependent of it) and must not overwrite
+    the scores that selection still reads.  Every call's lists equal the
+    workload's own."""
+    loads = [W.make_config(3), W.make_config(4)]
+    tens = [device_inputs(w) for w in loads]
+    refs = []
+    for w, t in zip(loads, tens):
+        _, ref, st = gpu_fused(w, t, in_workspace=True)
+        assert st == 0
+        refs.append(ref)
+    R = max(w.R for w in loads)
+    max_len = max(w.max_len for w in loads)
+    ws = binding.new_workspace(R, max_len, 2048, with_scores=True)
+    stream = torch.cuda.Stream()
+    outs = []
+    for i in range(6):
+        w, t = loads[i % 2], tens[i % 2]
+        idx = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+        binding.score_topk(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"], t["seq_lens"],
+                           t["row_req"], w.max_len, w.k, idx, ws, stream=stream)
+        outs.append(idx)
+    stream.synchronize()
+    assert binding.check_status(ws, stream) == 0
+    for i, idx in enumerate(outs):
+        assert np.array_equal(idx.cpu().numpy(), refs[i % 2]), "call %d" % i
+
+
 def test_host_buffer_call_error_inside_its_graph():
     """An argument error found while the host-buffer call captures its launches
     (a key cache that is not 16-byte aligned) is returned, ends the capture,
