@@ -237,10 +237,9 @@ idx_status idx_score_topk_host(int qtype, const void *q_host, const float *head_
  * idx_score_noalloc -- idx_score for callers that cannot allocate device
  * memory, with no workspace argument.  The indexer launch this library
  * follows has no counterpart to this entry point; it exists for callers such
- * as a serving loop replaying a
- * captured CUDA graph, an allocator-less embedding, or code inside a memory
- * pool that forbids new allocations, which cannot obtain (or size) a
- * workspace buffer.
+ * as a serving loop replaying a captured CUDA graph, an allocator-less
+ * embedding, or code inside a memory pool that forbids new allocations,
+ * which cannot obtain (or size) a workspace buffer.
  *
  * Arguments, layouts and results are those of idx_score minus the workspace.
  * Instead of a workspace, the call uses one fixed scratch array in device
