@@ -211,20 +211,20 @@ size_t idx_host_workspace_bytes(int R, int64_t max_len, int k, int n_req, int ma
  * it, or wait on an event recorded after the call), and the host must not
  * modify the inputs before then.
  *
- * When every buffer is mapped and `stream` is an explicit stream that is not
- * being captured, the call's launches run as one CUDA graph kept per host
- * thread: the launches are captured from `stream`, written into the thread's
- * executable graph (updated in place when only arguments change, else built
- * again) and launched with cudaGraphLaunch.  The first such call of a thread
- * launches directly.  Calls on the legacy or per-thread default stream, with
- * a pageable buffer, or under a caller's capture launch directly.  Launches
- * of one thread's graph run in order, whatever stream they are issued on.
+ * The gather kernel and the scoring kernel are programmatic dependents of
+ * the kernel before each on `stream` (as every scoring launch is): the gather
+ * may read the host buffers as soon as that kernel allows dependents to
+ * launch (this library's selection does so at its start; a kernel that never
+ * does simply completes first), and waits for it to complete before writing
+ * the workspace.  So the host buffers must hold this call's inputs when the
+ * call is made.
  *
  *  workspace  device memory, 1024-byte aligned, >= idx_host_workspace_bytes
  *             (R, max_len, k, n_req, max_pages), zeroed once by idx_workspace_init
  *
- * Errors: those of idx_score_topk; IDX_ERR_ARG for a null host pointer or a
- * size out of range, IDX_ERR_CUDA when a copy cannot be queued.
+ * Errors: those of idx_score_topk, all checked before anything is launched;
+ * IDX_ERR_ARG for a null host pointer or a size out of range, IDX_ERR_CUDA
+ * when a copy cannot be queued.
  */
 idx_status idx_score_topk_host(int qtype, const void *q_host, const float *head_w_host,
                                const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,

@@ -345,9 +345,11 @@ idx_status host_launches(const HostCall& c, cudaStream_t s) {
         return IDX_ERR_CUDA;
     }
     const HostLayout& H = c.H;
-    // (The scoring kernel launches as a programmatic dependent of the stage
-    // kernel: its CTAs set up while the stage runs and wait for it to finish
-    // before reading what it wrote.)
+    // The gather and the scoring kernel are each a programmatic dependent of
+    // the kernel before them: the gather reads the host buffers while the
+    // previous call's selection runs, the scoring's CTAs set up while the
+    // gather runs; each waits for its predecessor before writing (and the
+    // scoring before reading what the gather wrote).
     const idx_status st =
         idx_score_topk(c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale,
                        c.pool_pages, reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages,
@@ -363,64 +365,6 @@ idx_status host_launches(const HostCall& c, cudaStream_t s) {
     return IDX_OK;
 }
 
-// A call whose buffers are all mapped host memory runs as one CUDA graph: its
-// launches are captured from the stream, written into this host thread's
-// executable graph (cudaGraphExecUpdate keeps it when only the arguments
-// changed) and launched with one cudaGraphLaunch, which starts the kernels
-// with less device-side delay than three stream launches.  The executable
-// graph is kept for the life of the thread.
-struct HostGraph {
-    int dev = -1;
-    bool warm = false;  // an eager call of this thread has set up every kernel's attributes
-    cudaGraphExec_t exec = nullptr;
-};
-thread_local HostGraph host_graph;
-
-idx_status host_launches_graph(const HostCall& c, cudaStream_t s, int dev) {
-    HostGraph& hg = host_graph;
-    if (hg.dev != dev) {  // another device: start over (the old graph stays with its context)
-        hg = HostGraph{};
-        hg.dev = dev;
-    }
-    if (!hg.warm) {
-        const idx_status st = host_launches(c, s);
-        if (st == IDX_OK) hg.warm = true;
-        return st;
-    }
-    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return host_launches(c, s);
-    }
-    const idx_status st = host_launches(c, s);
-    cudaGraph_t g = nullptr;
-    const cudaError_t ec = cudaStreamEndCapture(s, &g);
-    if (st != IDX_OK || ec != cudaSuccess || g == nullptr) {
-        if (g) cudaGraphDestroy(g);
-        (void)cudaGetLastError();
-        if (st != IDX_OK) return st;  // an argument error: nothing was issued
-        return host_launches(c, s);   // the capture failed: run eagerly
-    }
-    if (hg.exec) {
-        cudaGraphExecUpdateResultInfo info;
-        if (cudaGraphExecUpdate(hg.exec, g, &info) != cudaSuccess) {
-            (void)cudaGetLastError();
-            cudaGraphExecDestroy(hg.exec);
-            hg.exec = nullptr;
-        }
-    }
-    if (!hg.exec && cudaGraphInstantiate(&hg.exec, g, 0) != cudaSuccess) {
-        (void)cudaGetLastError();
-        hg.exec = nullptr;
-        cudaGraphDestroy(g);
-        return host_launches(c, s);
-    }
-    cudaGraphDestroy(g);
-    if (cudaGraphLaunch(hg.exec, s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return IDX_ERR_CUDA;
-    }
-    return IDX_OK;
-}
 }  // namespace
 
 idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_w_host, const uint8_t* k_cache,
@@ -448,6 +392,15 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
     c.ws_bytes = ws_bytes;
     c.H = host_layout(R, max_len, k, n_req, max_pages);
     if (ws_bytes < c.H.end) return IDX_ERR_WORKSPACE;
+    // every argument check of the fused call, before anything is launched
+    const idx_status pre =
+        check_score_args(qtype, c.ws + c.H.q, reinterpret_cast<const float*>(c.ws + c.H.w), k_cache, k_scale,
+                         pool_pages, reinterpret_cast<const int32_t*>(c.ws + c.H.bt), max_pages,
+                         reinterpret_cast<const int32_t*>(c.ws + c.H.lens),
+                         reinterpret_cast<const int32_t*>(c.ws + c.H.rreq), R, workspace);
+    if (pre != IDX_OK) return pre;
+    if ((max_len < (int64_t)max_pages * kPage ? max_len : (int64_t)max_pages * kPage) > kSelectMaxLen)
+        return IDX_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Inputs in page-locked, mapped host memory are gathered by one kernel that
     // reads them over the host link; any other buffer is copied by the copy engine.
@@ -477,17 +430,6 @@ idx_status idx_score_topk_host(int qtype, const void* q_host, const float* head_
     c.idx_out = reinterpret_cast<int32_t*>(c.ws + c.H.idx);
     const void* out_map = mapped(indices_host);
     if (out_map && aligned(out_map, 4)) c.idx_out = const_cast<int32_t*>(static_cast<const int32_t*>(out_map));
-    // One graph when every buffer is mapped (no pageable copy, which a graph
-    // cannot hold) and the stream is an explicit one that is not capturing
-    // already (a caller's capture takes the launches as they are).
-    const bool all_mapped = c.n_copy == 0 && c.idx_out != reinterpret_cast<int32_t*>(c.ws + c.H.idx);
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusActive;
-    int dev = 0;
-    if (all_mapped && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread &&
-        cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
-        cudaGetDevice(&dev) == cudaSuccess)
-        return host_launches_graph(c, s, dev);
-    (void)cudaGetLastError();
     return host_launches(c, s);
 }
 

@@ -119,10 +119,11 @@ def test_host_buffer_call_matches_device_call(cfg, pinned):
 
 def test_host_buffer_calls_on_a_stream():
     """On an explicit stream with every buffer page-locked, idx_score_topk_host
-    runs each call as this thread's cached CUDA graph (updated per call): five
-    calls issued back to back with no synchronisation, alternating workloads
-    of different shapes and inputs, each into its own host indices, all give
-    the device call's lists."""
+    calls issued back to back with no synchronisation (each call's gather
+    reading its host inputs while the previous call's selection still runs),
+    alternating workloads of different shapes and inputs, each into its own
+    host indices and all through one workspace per shape, give the device
+    call's lists."""
     loads = [W.make_config(4), W.make_config(2), W.make_config(4, seed=44), W.make_config(1), W.make_config(4)]
     refs, args = [], []
     for w in loads:
@@ -136,7 +137,7 @@ def test_host_buffer_calls_on_a_stream():
         args.append((pin(w.q), pin(w.head_w), t["k_cache"], t["k_scale"], pin(w.block_table), pin(w.seq_lens),
                      pin(w.row_req), w.max_len, w.k, out, ws))
     stream = torch.cuda.Stream()
-    binding.score_topk_host(*args[0], stream=stream)  # the thread's first call on this path runs eagerly
+    binding.score_topk_host(*args[0], stream=stream)
     stream.synchronize()
     args[0][9].fill_(-7)
     for a in args:
@@ -178,11 +179,11 @@ def test_back_to_back_calls_share_a_workspace():
         assert np.array_equal(idx.cpu().numpy(), refs[i % 2]), "call %d" % i
 
 
-def test_host_buffer_call_error_inside_its_graph():
-    """An argument error found while the host-buffer call captures its launches
-    (a key cache that is not 16-byte aligned) is returned, ends the capture,
-    and leaves the stream and the thread's graph usable: the next call gives
-    the device call's lists."""
+def test_host_buffer_call_argument_error():
+    """An argument error of the fused call (a key cache that is not 16-byte
+    aligned) is returned by the host-buffer call before it launches anything,
+    and the stream stays usable: the next call gives the device call's
+    lists."""
     w = W.make_config(1)
     t = device_inputs(w)
     _, ref, st = gpu_fused(w, t)
@@ -199,8 +200,8 @@ def test_host_buffer_call_error_inside_its_graph():
                                        t["k_scale"].data_ptr(), t["k_cache"].shape[0], bt.data_ptr(),
                                        bt.shape[0], bt.shape[1], sl.data_ptr(), rq.data_ptr(), w.R, w.max_len,
                                        w.k, out.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
-    assert call(0) == 0 and call(0) == 0  # a direct call, then one through the thread's graph
-    assert call(1) == -2                   # IDX_ERR_ALIGN, raised inside the capture
+    assert call(0) == 0 and call(0) == 0
+    assert call(1) == -2                   # IDX_ERR_ALIGN
     with torch.cuda.stream(stream):
         assert not torch.cuda.is_current_stream_capturing()
     out.fill_(-7)
