@@ -621,6 +621,9 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         }
     }
 
+    // This CTA's scores are written: the selection (a programmatic dependent)
+    // may launch onto the SMs the scoring frees; it waits for the whole grid.
+    pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) record_status(p.status, kStatusTimeout);

@@ -326,6 +326,9 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     // up on the SMs this launch leaves free; it waits for this grid to finish
     // before it reads or writes anything in global memory.
     pdl_launch_dependents();
+    // This launch is itself a programmatic dependent of the kernel before it
+    // (the scoring): wait for that grid before reading a score.
+    pdl_wait();
 
     // Slice c covers positions [c * slice_cap, (c + 1) * slice_cap) of the row
     // (slice_cap is fixed by the launch's length bound), so its score loads
@@ -558,13 +561,16 @@ cudaError_t launch_c(const SelectArgs& a) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = slice_bytes(cap);
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // a programmatic dependent of the kernel before it (k_select waits for it)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const int64_t cap_len = a.len_cap < a.score_stride ? a.len_cap : a.score_stride;
     const SlotMap sm{a.slot_table, a.slot_row_req, a.slot_max_pages};
     return cudaLaunchKernelEx(&cfg, k_select<CL>, a.scores, cap_len, a.row_lens, a.score_stride, a.k, a.indices,
