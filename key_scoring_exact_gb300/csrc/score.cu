@@ -47,6 +47,13 @@
 //              quadrant) per warp: tcgen05.ld the row's 64 head columns, ReLU,
 //              head-weighted sum (packed f32x2 FMAs), times the key scale,
 //              masked coalesced f32 stores.
+//
+// Every launch is a programmatic dependent of the kernel before it on the
+// stream: its CTAs may start on SMs that kernel frees, set up barriers and
+// TMEM, and wait (griddepcontrol.wait) before touching global memory; each
+// CTA allows the next launch (the selection) once its scores are written.
+// Launches of many tiles per CTA use a second instantiation whose epilogue
+// keeps half of its row's head weights in registers (kRegW below).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 

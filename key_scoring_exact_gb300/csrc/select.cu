@@ -9,11 +9,16 @@
 //
 // GB300 form:
 //  * A row is one thread-block cluster of 16, 8, 4, 2 or 1 CTAs, the size
-//    chosen per launch (the largest whose slices hold the longest row and
-//    whose clusters for all rows are resident at once).  The slices are the
+//    chosen per launch (one CTA when the longest row has at most 12,288
+//    keys; otherwise the largest whose slices hold the longest row and whose
+//    clusters for all rows are resident at once).  The slices are the
 //    cluster's CTAs; slice c covers positions [c P, (c + 1) P) with P fixed by
 //    the launch's length bound, so its score loads go out together with the
 //    read of the row's length; a row of at most P keys runs on one CTA alone.
+//  * The launch is a programmatic dependent of the kernel before it (the
+//    scoring): it waits for that grid before reading a score, and at once
+//    allows the next launch (the next scoring) to start on the SMs it leaves
+//    free.
 //  * A slice's keys live in shared memory, as the order-preserving uint32
 //    image of the f32 score (-0 folded into +0, NaN below every number).
 //  * Digits of 11, 11 and 10 bits: three rounds give the exact k-th largest
