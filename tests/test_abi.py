@@ -98,3 +98,13 @@ def test_host_entry_sizes_and_argument_errors(lib):
     odd = list(args)
     odd[15] = ctypes.c_void_p(1024 + 256)
     assert lib.idx_score_topk_host(*odd) == -2                   # workspace alignment
+    # the fused call's own checks also run before anything is launched
+    kc = list(args)
+    kc[3] = ctypes.c_void_p(1024 + 1)
+    assert lib.idx_score_topk_host(*kc) == -2                    # key cache alignment
+    pool = list(args)
+    pool[5] = 0
+    assert lib.idx_score_topk_host(*pool) == -1                  # empty page pool
+    long_rows = list(args)
+    long_rows[8], long_rows[12] = 10000, 600000                  # rows past the selection's 524,288 keys
+    assert lib.idx_score_topk_host(*long_rows) == -1
