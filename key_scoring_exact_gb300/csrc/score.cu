@@ -75,7 +75,7 @@ constexpr uint32_t kPageScaleBytes = kPage * 4;            // 256 B
 constexpr uint32_t kStageBytes = kTileKeys * kDim;         // 16 KB
 constexpr uint32_t kStageScaleBytes = kTileKeys * 4;       // 512 B
 constexpr uint32_t kAccCols = 256;
-constexpr int kRegWTilesPerCta = 32;  // launches of at least this many tiles per CTA keep weights in registers
+constexpr int kRegWTilesPerCta = 12;  // launches of at least this many tiles per CTA keep weights in registers
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 
 constexpr uint32_t kOffQHi = 0;
@@ -670,7 +670,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
     // Tiles per CTA, at least (the rows form at least ceil(R / 4) groups, each
-    // of up to len_cap keys): the register-held weights from 32 on.
+    // of up to len_cap keys): the register-held weights from 12 on.
     const int64_t tiles = (int64_t)((a.R + kGroupRows - 1) / kGroupRows) * ((p.len_cap + kTileKeys - 1) / kTileKeys);
     const bool reg_w = tiles >= (int64_t)kRegWTilesPerCta * a.num_sms;
     cudaLaunchConfig_t cfg = {};
