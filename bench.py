@@ -8,11 +8,16 @@ with per-key scales whose last 4,096 keys are 8x, bf16 query, 64 heads x 128,
 k = 2048).  Successive steps cycle through enough copies of the key cache
 to exceed 2.1 x L2 (17 copies, 294 MB), so keys stream from HBM.
 
-Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
-graphs, bracketed by CUDA events on the launching stream (and a barrier +
-max over ranks under torchrun).  For the per-kernel roofline, each of the two
-kernels is then replayed alone from a graph of its own launches, bracketed by
-CUDA events.  nvidia-smi samples the clocks during the timed steps.
+Timing: W untimed warm-up steps, then about 0.8 s of untimed replays while
+nvidia-smi starts sampling the clocks, then 7 trials of exactly K steps
+replayed from CUDA graphs (a barrier + max over ranks under torchrun); each
+trial is bracketed by CUDA events on the launching stream, behind a short
+idle kernel so the host has queued the trial before the first event, and the
+reported time per step is the median over the trials.  For the per-kernel
+roofline, each of the two kernels is then replayed alone from a graph of its
+own launches, bracketed by CUDA events.  The FP8 tensor-core rate the scoring
+is measured against comes from idx_probe_fp8_mma on the same GPU in the same
+run.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
 plain f64 scoring and sort-based selection) on a bounded sample.
@@ -38,15 +43,15 @@ METRIC = "µs per indexer launch (score + exact top-2048) at 4 rows, 8K/128K key
 UNIT = "us"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio
 L2_BYTES = 129 * 1024 * 1024
 COPIES = 16
+TRIALS = 7
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, help="workload configuration 1..5")
@@ -156,6 +161,38 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def fp8_peak(stream, tries: int = 3) -> dict:
+    """The FP8 tcgen05 MMA rate of this GPU, measured now: the best of a few
+    runs of idx_probe_fp8_mma (M = 128 x N = 256 x K = 32, the scoring's MMA
+    shape, back to back on every SM)."""
+    from key_scoring_exact_gb300 import binding
+    best = None
+    for _ in range(tries):
+        r = binding.probe_fp8_mma(8192, 256, stream=stream)
+        if best is None or r["tflops"] > best["tflops"]:
+            best = r
+    best["source"] = "idx_probe_fp8_mma in this run (best of %d)" % tries
+    return best
+
+
+def mma_roofline(st, t_score: float, hbm_floor_s: float, fp8: dict) -> dict:
+    """The scoring's tensor-core side: algorithmic flops (2 * 64 * 128 per
+    row-key) and the flops the MMAs execute (twice that for a bf16 query,
+    split exactly into two E4M3 terms), each against the measured FP8 rate,
+    and which floor binds the kernel."""
+    alg = st.alg_flops()
+    executed = alg * (1 if st.w.q_is_e4m3 or st.quantize_q else 2)
+    peak = fp8["tflops"] * 1e12
+    floors = {"hbm_us": hbm_floor_s * 1e6, "mma_alg_us": alg / peak * 1e6, "mma_executed_us": executed / peak * 1e6}
+    binding_floor = max(floors, key=floors.get)
+    return {"alg_flops": alg, "executed_flops": executed, "fp8_peak_tflops": fp8["tflops"],
+            "fp8_peak_source": fp8["source"], "fp8_ns_per_mma": fp8["ns_per_mma"], "fp8_probe_mhz": fp8["mhz"],
+            "alg_tflops": alg / t_score / 1e12, "executed_tflops": executed / t_score / 1e12,
+            "alg_frac": alg / t_score / peak, "executed_frac": executed / t_score / peak,
+            "floors": floors, "binding_floor": binding_floor,
+            "frac_of_binding_floor": floors[binding_floor] / 1e6 / t_score}
+
+
 def ncu_traffic(kernel: str, source: str):
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
     summary, or None when the kernel's source has changed since the capture."""
@@ -240,33 +277,65 @@ def capture(stream, fn, n):
     return g
 
 
-def time_graph_steps(st: Step, steps: int, stream, dist, sampler=None):
-    """Exactly `steps` fused steps replayed from graphs; returns seconds per step."""
-    G = min(steps, 256)
-    full, rem = divmod(steps, G)
-    g_full = capture(stream, lambda i: st.fused(i, stream), G)
-    g_rem = capture(stream, lambda i: st.fused(i, stream), rem) if rem else None
-    g_full.replay()  # upload + warm
-    if g_rem is not None:
-        g_rem.replay()
+def _idle(stream, us: float = 100.0):
+    """A short spin kernel on the stream: while it runs, the host queues the
+    next trial, so the trial's first event is not followed by launch latency."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2000))
+
+
+def time_graph_steps(st: Step, steps: int, stream, dist, sampler=None, trials: int = TRIALS,
+                     settle_s: float = 0.8):
+    """`trials` timed trials of exactly `steps` fused steps each, replayed from
+    CUDA graphs and bracketed by CUDA events on the launching stream.
+    Consecutive steps use consecutive key-cache copies (trials of up to 256
+    steps continue the rotation where the previous trial stopped).  With a
+    sampler, the clocks are sampled from `settle_s` seconds of untimed replays
+    before the first trial until the last one ends.  Returns (median seconds
+    per step over the trials, per-trial seconds per step)."""
+    G = 255 // st.copies * st.copies if st.copies <= 255 else st.copies  # a whole number of rotations
+    cache = {}
+
+    def graph(n, start):
+        key = (n, start % st.copies)
+        if key not in cache:
+            cache[key] = capture(stream, lambda i: st.fused(start + i, stream), n)
+        return cache[key]
+
+    plan = []
+    for t in range(trials):
+        if steps <= 256:
+            plan.append([graph(steps, t * steps)])   # one graph; the rotation continues across trials
+        else:
+            full, rem = divmod(steps, G)             # starts at copy 0
+            plan.append([graph(G, 0)] * full + ([graph(rem, 0)] if rem else []))
+    for gl in plan:                                  # upload + warm every graph
+        for g in gl:
+            g.replay()
     torch.cuda.synchronize()
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler is not None:
         sampler.start()
-    e0.record(stream)
-    for _ in range(full):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record(stream)
+        t_end = time.perf_counter() + settle_s
+        while time.perf_counter() < t_end:
+            for g in plan[0]:
+                g.replay()
+            torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in plan]
+    for (e0, e1), gl in zip(ev, plan):
+        _idle(stream)
+        e0.record(stream)
+        for g in gl:
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     if sampler is not None:
         sampler.stop()
     barrier(dist)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / steps
+    per = [e0.elapsed_time(e1) / 1e3 / steps for e0, e1 in ev]
+    return statistics.median(per), per
 
 
 def per_kernel_times(st: Step, n: int, stream):
@@ -339,32 +408,64 @@ def e2e_time(st: Step, steps: int, stream):
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def _oracle_run(w, keys_per_row: int):
-    """Oracle scores of every row over its first keys_per_row keys, then the
-    sort-based top-k of those scores.  Returns (seconds, row-keys done)."""
+def _oracle_problem(w, keys_per_row: int):
     import oracle
     lens = w.seq_lens.numpy()
     sample = np.minimum(lens, max(1, int(keys_per_row))).astype(np.int32)
     pb = oracle.Problem(w.q_bits().numpy(), w.q_is_e4m3, w.head_w.numpy(), w.k_cache.numpy(),
                         w.k_scale.numpy(), w.block_table.numpy(), sample, w.row_req.numpy())
-    t0 = time.perf_counter()
-    s = oracle.scores(pb)
+    return pb, sample
+
+
+def _oracle_run(w, keys_per_row: int, threads: int = 1):
+    """Oracle scores of every row over its first keys_per_row keys, then the
+    sort-based top-k of those scores.  With threads > 1 the unchanged oracle
+    calls run on a pool of host threads (the C oracle releases the GIL):
+    scores over (row, key-chunk) tasks, then one top-k per row.  Returns
+    (seconds, row-keys done)."""
+    import oracle
+    pb, sample = _oracle_problem(w, keys_per_row)
+    if threads <= 1:
+        t0 = time.perf_counter()
+        s = oracle.scores(pb)
+        for r in range(w.R):
+            oracle.topk(s[r, :sample[r]].astype(np.float32), w.k)
+        return time.perf_counter() - t0, int(sample.sum())
+    from concurrent.futures import ThreadPoolExecutor
+    tasks = []
     for r in range(w.R):
-        oracle.topk(s[r, :sample[r]].astype(np.float32), w.k)
+        n = int(sample[r])
+        chunk = max(64, -(-n * w.R // (4 * threads)))
+        tasks += [(r, a, min(n, a + chunk)) for a in range(0, n, chunk)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda t: oracle.score_positions(pb, t[0], np.arange(t[1], t[2])), tasks))
+        rows = [np.concatenate([p for t, p in zip(tasks, parts) if t[0] == r] or [np.zeros(0)])
+                for r in range(w.R)]
+        list(ex.map(lambda r: oracle.topk(rows[r].astype(np.float32), w.k), range(w.R)))
     return time.perf_counter() - t0, int(sample.sum())
 
 
-def oracle_launch_time(w, budget_s: float):
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_launch_time(w, budget_s: float, threads: int = 1):
     """The oracle as it stands, timed on a bounded sample sized to take about
-    budget_s seconds, scaled to one whole launch (per row-key).  Single-threaded."""
+    budget_s seconds of CPU work, scaled to one whole launch (per row-key),
+    on `threads` host threads."""
     lens = w.seq_lens.numpy()
-    t, done = _oracle_run(w, 256)                       # calibration
+    t, done = _oracle_run(w, 256)                       # calibration, one thread
     per_rowkey = t / done
     keys = int(min(lens.max(), max(256, budget_s / per_rowkey / w.R)))
-    t, done = _oracle_run(w, keys)
+    t, done = _oracle_run(w, keys, threads)
     total = float(lens.sum())
     desc = ("all %d rows over their first %d keys: %d of %d row-keys (%.3g of the launch), "
-            "time scaled by row-keys" % (w.R, keys, done, int(total), done / total))
+            "time scaled by row-keys, %d host thread%s" % (w.R, keys, done, int(total), done / total, threads,
+                                                          "" if threads == 1 else "s"))
     return t * total / done, desc
 
 
@@ -374,10 +475,11 @@ def reference_main(args, w):
         return
     # the whole run (warm-up + steps) stays within about two minutes
     per_step = max(0.02, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    cores = host_cores()
     times = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        t, desc = oracle_launch_time(w, per_step)
+        t, desc = oracle_launch_time(w, per_step * cores, cores)
         if i >= args.warmup:
             times.append(t)
     us = float(np.mean(times)) * 1e6
@@ -385,7 +487,7 @@ def reference_main(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_desc(w, args),
-            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -403,6 +505,7 @@ def main():
     args = parse()
     from key_scoring_exact_gb300 import workloads as W
     w = W.make_config(args.config)
+    args.copies = copies_for(w, args.copies)   # the same rotation (and config line) in both arms
     if args.impl == "reference":
         reference_main(args, w)
         return
@@ -415,7 +518,6 @@ def main():
     from key_scoring_exact_gb300 import binding
     binding.load(build_if_missing=True)
     stream = torch.cuda.Stream(device=dev)
-    args.copies = copies_for(w, args.copies)
     st = Step(w, args.copies, dev)
 
     sampler = ClockSampler(local)
@@ -425,7 +527,7 @@ def main():
         torch.cuda.synchronize()
         if binding.check_status(st.ws, stream) != 0:
             raise RuntimeError("device status after warm-up")
-        sec = time_graph_steps(st, args.steps, stream, dist, sampler)
+        sec, trial_secs = time_graph_steps(st, args.steps, stream, dist, sampler)
     clocks = sampler.result
     sec = max_over_ranks(dist, sec)
     with torch.cuda.stream(stream):
@@ -435,6 +537,8 @@ def main():
         raise RuntimeError("device status %d after the timed steps" % status)
 
     hbm, bf16, bf16_sus, src = peaks()
+    with torch.cuda.stream(stream):
+        fp8 = fp8_peak(stream)
     score_bytes = st.alg_bytes_score()
     select_bytes = st.alg_bytes_select()
     roof_score = {"kernel": "k_score", "bound": "hbm",
@@ -458,10 +562,12 @@ def main():
         "roofline_other": other,
         "roofline_fused": {"alg_bytes": fused_bytes, "roof_us": fused_bytes / hbm / 1e3,
                            "frac": fused_bytes / hbm / 1e3 / (sec * 1e6)},
-        "mma": {"alg_flops": st.alg_flops(), "executed_flops": st.alg_flops() * (1 if w.q_is_e4m3 else 2),
-                "fp8_peak_tflops": bf16 * FP8_OVER_BF16,
-                "alg_tflops_in_scoring": st.alg_flops() / t_score / 1e12},
-        "gpu_launches": 2 * args.steps,
+        "mma": mma_roofline(st, t_score, score_bytes / (hbm * 1e9), fp8),
+        "trials": {"n": len(trial_secs), "steps_each": args.steps,
+                   "per_step_us": [round(x * 1e6, 3) for x in trial_secs],
+                   "mean_us": float(np.mean(trial_secs)) * 1e6, "statistic": "median"},
+        "gpu_launches": 2 * args.steps,           # per timed trial (scoring + selection per step)
+        "gpu_launches_all_trials": 2 * args.steps * len(trial_secs),
         "clocks": clocks,
     }
     if not args.no_8k:
@@ -470,7 +576,7 @@ def main():
         with torch.cuda.stream(stream):
             for i in range(3):
                 st8.fused(i, stream)
-            sec8 = time_graph_steps(st8, min(args.steps, 1024), stream, None)
+            sec8, _ = time_graph_steps(st8, min(args.steps, 1024), stream, None)
         line["also_8k"] = {"workload": w8.recipe, "us": sec8 * 1e6,
                            "keys_per_s": w8.row_keys() / sec8}
         del st8
@@ -481,7 +587,7 @@ def main():
         with torch.cuda.stream(stream):
             for i in range(3):
                 stw.fused(i, stream)
-            secw = time_graph_steps(stw, min(args.steps, 4096), stream, None)
+            secw, _ = time_graph_steps(stw, min(args.steps, 4096), stream, None)
         line["also_warm_l2"] = {"workload": w.recipe + "; one key-cache copy, resident in L2 between steps",
                                 "us": secw * 1e6, "keys_per_s": w.row_keys() / secw}
         del stw
@@ -492,7 +598,7 @@ def main():
         with torch.cuda.stream(stream):
             for i in range(3):
                 stb.fused(i, stream)
-            secb = time_graph_steps(stb, min(args.steps, 64), stream, None)
+            secb, _ = time_graph_steps(stb, min(args.steps, 64), stream, None)
             tb_score, tb_select = per_kernel_times(stb, min(args.steps, 32), stream)
         line["also_64_rows"] = {"workload": wb.recipe, "us": secb * 1e6, "scoring_us": tb_score * 1e6,
                                 "selection_us": tb_select * 1e6,
@@ -506,7 +612,7 @@ def main():
         with torch.cuda.stream(stream):
             for i in range(3):
                 st.fused(i, stream)
-            secq = time_graph_steps(st, min(args.steps, 4096), stream, None)
+            secq, _ = time_graph_steps(st, min(args.steps, 4096), stream, None)
             tq_score, _ = per_kernel_times(st, min(args.steps, 256), stream)
         st.quantize_q = False
         line["also_fp8_query"] = {"workload": w.recipe + "; query quantised to E4M3 on the device per (row, head)",
@@ -517,8 +623,11 @@ def main():
         line["e2e"] = {"value": e2e_sec * 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h}
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        t, desc = oracle_launch_time(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": t * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        cores = host_cores()
+        t1, desc1 = oracle_launch_time(w, args.cpu_seconds)
+        tn, descn = oracle_launch_time(w, args.cpu_seconds, cores)
+        line["cpu_baseline"] = {"value": tn * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": descn,
+                                "one_core": {"value": t1 * 1e6, "cores": 1, "sample": desc1}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -125,7 +125,8 @@ idx_status idx_score(int qtype, const void *q, const float *head_w,
  *  k            1 .. IDX_MAX_K
  *  indices      [R][k] int32 out
  *  workspace    status word holder (>= idx_workspace_bytes(R, score_stride, k, 0)
- *               bytes); may be NULL, then device errors are not reported
+ *               bytes, else IDX_ERR_WORKSPACE); may be NULL, then device errors
+ *               are not reported
  *
  * Errors: IDX_ERR_ARG, IDX_ERR_ALIGN, IDX_ERR_WORKSPACE, IDX_ERR_CUDA.
  */
@@ -249,8 +250,10 @@ idx_status idx_score_topk_host(int qtype, const void *q_host, const float *head_
  * library routine.
  *
  *  - R must be in [1, IDX_NOALLOC_MAX_ROWS]; larger R returns IDX_ERR_ARG.
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - The first call in a CUDA context (normally a device's primary context)
+ *    looks up the array's device address with that context current; make
+ *    that first call before any stream capture.  After a device reset the
+ *    next call looks the address up again.
  *  - All calls share the one array.  Calls whose work overlaps on the GPU
  *    (different streams without ordering, or several host threads) share its
  *    status word; nothing else is shared, and nothing needs clearing.

@@ -23,6 +23,7 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
            "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots")
+DIAG_EXPORTS = ("idx_probe_fp8_mma", "idx_test_set_wait_limit")   # include/idx_diag.h
 
 _lib = None
 
@@ -76,6 +77,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_host_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
     lib.idx_score_topk_host.restype = i32
     lib.idx_score_topk_host.argtypes = [i32, p, p, p, p, i64, p, i32, i32, p, p, i32, i64, i32, p, p, sz, p]
+    lib.idx_probe_fp8_mma.restype = i32
+    lib.idx_probe_fp8_mma.argtypes = [i32, i32, p, p, i32, p]
+    lib.idx_test_set_wait_limit.restype = i32
+    lib.idx_test_set_wait_limit.argtypes = [ctypes.c_ulonglong, i32]
     _lib = lib
     return lib
 
@@ -278,3 +283,29 @@ def scores_view(workspace: torch.Tensor, R: int, max_len: int) -> torch.Tensor:
     stride = max(4, (int(max_len) + 3) // 4 * 4)
     n = R * stride
     return workspace[no_scores:no_scores + 4 * n].view(torch.float32).view(R, stride)
+
+
+def probe_fp8_mma(n_mma: int = 8192, n_cols: int = 256, stream=None) -> dict:
+    """idx_probe_fp8_mma: back-to-back tcgen05 FP8 MMAs (M = 128, N = n_cols,
+    K = 32) on every SM; returns the device's rate and the per-MMA time."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ns = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    clk = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    _check(load().idx_probe_fp8_mma(int(n_mma), int(n_cols), ns.data_ptr(), clk.data_ptr(), sms, _stream(stream)),
+           "idx_probe_fp8_mma")
+    torch.cuda.synchronize()
+    ns_h, clk_h = ns.cpu().tolist(), clk.cpu().tolist()
+    if min(ns_h) <= 0:
+        raise RuntimeError("idx_probe_fp8_mma: a CTA's wait gave up")
+    worst = max(ns_h)
+    flops = 2.0 * 128 * n_cols * 32 * n_mma * sms
+    return {"tflops": flops / (worst * 1e-9) / 1e12, "ns_per_mma": worst / n_mma,
+            "clk_per_mma": max(clk_h) / n_mma, "sms": sms, "n_mma": n_mma, "n_cols": n_cols,
+            "mhz": max(clk_h) / worst * 1e3}
+
+
+def test_set_wait_limit(wait_ns: int, drop_query_handoff: bool = False) -> None:
+    """idx_test_set_wait_limit (test only): this thread's later scoring
+    launches give up waiting after wait_ns (0 = the normal 2 s); with
+    drop_query_handoff the kernel's query hand-off is never signalled."""
+    _check(load().idx_test_set_wait_limit(int(wait_ns), 1 if drop_query_handoff else 0), "idx_test_set_wait_limit")

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libidx.so")
-SOURCES = ["idx_api.cu", "score.cu", "select.cu", "stage.cu", "quant.cu"]
+SOURCES = ["idx_api.cu", "score.cu", "select.cu", "stage.cu", "quant.cu", "diag.cu"]
 HEADERS = ["idx_internal.h", "ptx.cuh", "quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
@@ -30,8 +30,8 @@ def nvcc() -> str:
 
 
 def _inputs():
-    inc = os.path.join(os.path.dirname(HERE), "include", "idx.h")
-    return [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [inc]
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    return [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(inc, h) for h in ("idx.h", "idx_diag.h")]
 
 
 def _stale() -> bool:

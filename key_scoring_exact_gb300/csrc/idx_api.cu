@@ -115,27 +115,63 @@ constexpr size_t kNoallocScratchBytes = 1024;  // the status word's block of the
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// The array's device address, looked up once per device with that device
-// current (in host code the array's name is only a stand-in for it).
+// The current CUDA context's unique id (driver entry points fetched at run
+// time: the library does not link the driver library); 0 when unavailable.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+        (void)cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// The array's device address in the current context (in host code the
+// array's name is only a stand-in for it), looked up once per context with
+// that context current: a device reset or another context gets a lookup of
+// its own, so no address outlives the context it belongs to.  Without a
+// context id the address is looked up on every call (that allocates nothing).
 idx_status noalloc_scratch(char** out) {
     static std::mutex mu;
-    static char* addr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    constexpr int kSlots = 16;
+    static unsigned long long ids[kSlots] = {0};
+    static char* addrs[kSlots] = {nullptr};
+    static int next = 0;
+    unsigned long long id = current_context_id();  // 0 before the device's context is made current
+    std::lock_guard<std::mutex> lock(mu);
+    if (id != 0)
+        for (int i = 0; i < kSlots; ++i)
+            if (ids[i] == id) {
+                *out = addrs[i];
+                return IDX_OK;
+            }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {  // makes the context current
         (void)cudaGetLastError();
         return IDX_ERR_CUDA;
     }
-    if (dev < 0 || dev >= 64) return IDX_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            (void)cudaGetLastError();
-            return IDX_ERR_CUDA;
-        }
-        addr[dev] = static_cast<char*>(p);
+    if (id == 0) id = current_context_id();
+    if (id != 0) {
+        ids[next] = id;
+        addrs[next] = static_cast<char*>(p);
+        next = (next + 1) % kSlots;
     }
-    *out = addr[dev];
+    *out = static_cast<char*>(p);
     return IDX_OK;
 }
 
@@ -263,7 +299,7 @@ idx_status idx_topk(const float* scores, int64_t score_stride, const int32_t* ro
     if (score_stride < 4 || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
     uint32_t* status = nullptr;
     if (workspace) {
-        if (ws_bytes < 256) return IDX_ERR_WORKSPACE;
+        if (ws_bytes < ws_layout(R, score_stride, 0).end) return IDX_ERR_WORKSPACE;
         status = static_cast<uint32_t*>(workspace);
     }
     DeviceInfo dev;

@@ -69,6 +69,16 @@ struct ScoreArgs {
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);
 
+// Test hook of the calling host thread (diag.cu): a wall-time limit for the
+// scoring kernel's waits (0 = the normal kWaitTimeoutNs) and whether the
+// epilogue leaves out its signal that the query operand is written, so that
+// a test can make a bounded wait run out without a fault.
+struct WaitTestHook {
+    uint64_t wait_ns;
+    int drop_query_handoff;
+};
+WaitTestHook wait_test_hook();
+
 struct SelectArgs {
     const float* scores;
     int64_t score_stride;

@@ -1,9 +1,10 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA / bulk
 // copies, tcgen05 (TMEM allocation, MMA, commit, loads), global timer.
 //
-// Every wait in this library is bounded: bounded_wait() gives up after
-// kWaitTimeoutNs of wall time (or when the CTA's abort flag is raised) so a
-// broken hand-off ends the kernel with an error status instead of a hang.
+// Every wait in this library is bounded: bounded_wait() gives up after a
+// wall-time limit (kWaitTimeoutNs unless a test asks for a shorter one) or
+// when the CTA's abort flag is raised, so a broken hand-off ends the kernel
+// with an error status instead of a hang.
 #pragma once
 
 #include <cstdint>
@@ -89,14 +90,17 @@ IDX_DEVI bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false (and raises *abort) when the deadline passes or *abort is already set.
-IDX_DEVI bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// false (and raises *abort) when `limit_ns` of wall time pass or *abort is
+// already set.
+IDX_DEVI bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                           uint64_t limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = limit_ns < 200000ull ? (uint32_t)limit_ns : 200000u;
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             return false;
         }

@@ -109,6 +109,8 @@ struct ScoreParams {
     float* scores;
     int64_t score_stride;
     uint32_t* status;
+    uint64_t wait_ns;        // wall-time limit of every role's waits (kWaitTimeoutNs in normal use)
+    int drop_query_handoff;  // test only: the epilogue never signals the query operand
 };
 
 struct PlanSmem {
@@ -439,7 +441,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 const int id1 = __shfl_sync(0xFFFFFFFFu, id, 2 * b + 1);
                 if (lane == 0) {
                     const int s = issued % kStages;
-                    if (!bounded_wait(&empty[s], ((issued / kStages) & 1) ^ 1, abort_flag)) {
+                    if (!bounded_wait(&empty[s], ((issued / kStages) & 1) ^ 1, abort_flag, p.wait_ns)) {
                         stop = true;
                     } else {
                         const uint32_t bytes = (id0 >= 0 ? kPageKeyBytes + kPageScaleBytes : 0u) +
@@ -483,14 +485,14 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                     while (g + 1 < n_groups && it >= pl.item[g + 1]) ++g;
                     gend = pl.item[g + 1];
                     // the epilogue has written this group's query operand
-                    if (!bounded_wait(qfull, qi & 1, abort_flag)) break;
+                    if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) break;
                     tc_fence_after_sync();
                     idesc = idesc_e4m3_f32(128, (uint32_t)pl.nr[g] * kHeads);
                     ++qi;
                 }
-                if (!bounded_wait(&tempty[li & 1], ((li >> 1) & 1) ^ 1, abort_flag)) break;
+                if (!bounded_wait(&tempty[li & 1], ((li >> 1) & 1) ^ 1, abort_flag, p.wait_ns)) break;
                 tc_fence_after_sync();
-                if (!bounded_wait(&full[li % kStages], (li / kStages) & 1, abort_flag)) break;
+                if (!bounded_wait(&full[li % kStages], (li / kStages) & 1, abort_flag, p.wait_ns)) break;
                 const uint32_t d = tmem_base + (uint32_t)(li & 1) * kAccCols;
                 const uint32_t a = a0 + (uint32_t)(li % kStages) * kStageBytes;
                 for (int k = 0; k < nmma; ++k) {  // K slice k % 4 of the hi (k < 4) or lo term
@@ -530,8 +532,8 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 split_group_query(p, r0, nr, q_hi, q_lo, wbuf, e, lane);
                 fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's operand reads
                 __syncwarp();
-                if (lane == 0) mbar_arrive(qfull);
-                if (!bounded_wait(qfull, qi & 1, abort_flag)) break;  // every warp's w' is written
+                if (lane == 0 && !p.drop_query_handoff) mbar_arrive(qfull);
+                if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) break;  // every warp's w' is written
                 w = wbuf + rr * kHeads;
                 if constexpr (kRegW) {
 #pragma unroll
@@ -544,12 +546,12 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 ++qi;
             }
             const int s = li % kStages, acc = li & 1;
-            if (!bounded_wait(&tfull[acc], (li >> 1) & 1, abort_flag)) break;
+            if (!bounded_wait(&tfull[acc], (li >> 1) & 1, abort_flag, p.wait_ns)) break;
             tc_fence_after_sync();
             // The stage cannot be refilled before this warp releases it, so its
             // `full` phase is still the current one: observe it, then read the
             // scales the bulk copy wrote.
-            if (!bounded_wait(&full[s], (li / kStages) & 1, abort_flag)) break;
+            if (!bounded_wait(&full[s], (li / kStages) & 1, abort_flag, p.wait_ns)) break;
             const float sc = scales[s * kTileKeys + key];
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -669,6 +671,9 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.scores = a.scores;
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
+    const WaitTestHook hook = wait_test_hook();
+    p.wait_ns = hook.wait_ns ? hook.wait_ns : kWaitTimeoutNs;
+    p.drop_query_handoff = hook.drop_query_handoff;
     // Tiles per CTA, at least (the rows form at least ceil(R / 4) groups, each
     // of up to len_cap keys): the register-held weights from 12 on.
     const int64_t tiles = (int64_t)((a.R + kGroupRows - 1) / kGroupRows) * ((p.len_cap + kTileKeys - 1) / kTileKeys);

@@ -10,12 +10,13 @@ from key_scoring_exact_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "idx.h")
+DIAG_HEADER = os.path.join(ROOT, "include", "idx_diag.h")
 
 
-def _declared():
-    text = open(HEADER).read()
+def _declared(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(idx_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(idx_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -31,9 +32,26 @@ def test_header_declares_the_api():
     assert set(names) == set(binding.EXPORTS)
 
 
+def test_diag_header_declares_the_diagnostics():
+    assert set(_declared(DIAG_HEADER)) == set(binding.DIAG_EXPORTS)
+
+
 def test_every_declared_symbol_is_exported(lib):
-    for name in _declared():
+    for name in _declared() + _declared(DIAG_HEADER):
         assert hasattr(lib, name), name
+
+
+def test_diag_argument_errors_need_no_gpu(lib):
+    lib.idx_probe_fp8_mma.restype = ctypes.c_int
+    p = ctypes.c_void_p
+    lib.idx_probe_fp8_mma.argtypes = [ctypes.c_int, ctypes.c_int, p, p, ctypes.c_int, p]
+    fake = ctypes.c_void_p(1024)
+    assert lib.idx_probe_fp8_mma(4, 256, fake, fake, 200, None) == -1      # too few MMAs
+    assert lib.idx_probe_fp8_mma(64, 250, fake, fake, 200, None) == -1     # N not a multiple of 16
+    assert lib.idx_probe_fp8_mma(64, 256, None, fake, 200, None) == -1     # null output
+    lib.idx_test_set_wait_limit.restype = ctypes.c_int
+    lib.idx_test_set_wait_limit.argtypes = [ctypes.c_ulonglong, ctypes.c_int]
+    assert lib.idx_test_set_wait_limit(0, 0) == 0
 
 
 def test_host_only_calls(lib):
