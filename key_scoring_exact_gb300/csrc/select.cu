@@ -21,9 +21,9 @@
 //    free.
 //  * A slice's keys live in shared memory, as the order-preserving uint32
 //    image of the f32 score (-0 folded into +0, NaN below every number).
-//  * Digits of 11, 11 and 10 bits: three rounds give the exact k-th largest
-//    image T and the number kr of keys equal to T that the list takes.  The
-//    first round's histogram is built while the slice is loaded.
+//  * Digits of 11, 11 and 10 bits give the exact k-th largest image T and
+//    the number kr of keys equal to T that the list takes.  The first
+//    round's histogram is built while the slice is loaded.
 //  * Histograms are built in shared memory with plain atomic adds (on this
 //    hardware faster than aggregating equal digits within a warp first, even
 //    when the scores crowd into a few bins).  The slices' histograms are
@@ -33,14 +33,25 @@
 //    barrier each thread reads its four bins' totals from their owner with
 //    one 16-byte remote load, then the block scans them.  No slice spins on
 //    another; every wait is a cluster barrier.
-//  * In the last round each thread scans its own contiguous run of the
-//    slice's positions, counting its keys above the 22-bit prefix and marking
-//    those that match it; each slice sends its count above the prefix and its
+//  * Leader path (a split row whose first digit's threshold bin holds at
+//    most kLeadCap keys, the usual case): each thread scans its own run of
+//    positions once, counting its keys above that bin and marking those in
+//    it; the marked keys (the candidates) go to the leader, the last slice,
+//    as (radix key, row position) pairs, with each slice's count above the
+//    bin.  After one cluster barrier the leader finds the two lower digits
+//    among the candidates with its own barriers only (one pass when the
+//    second digit's bin holds a single candidate, which is then T), counts
+//    each slice's candidates above and at T, and sends every slice T, kr and
+//    the keys above / at T in the slices before it; one more cluster barrier
+//    and every slice writes its part of the list.
+//  * Otherwise two more cluster rounds: in the last one each thread scans its
+//    own run, counting its keys above the 22-bit prefix and marking those
+//    that match it; each slice sends its count above the prefix and its
 //    non-zero last-digit bins (at most 8 of them) to the other slices with the
 //    round's histogram, so after that round's barrier every slice knows how
 //    many keys above T and at T the slices before it hold.  Only when some
 //    slice has more non-zero bins does one more exchange (and barrier) follow.
-//    One block scan of the threads' packed (above T, at T) counts gives their
+//  * One block scan of the threads' packed (above T, at T) counts gives their
 //    offsets, and the positions are written in order: keys above T first,
 //    then ties, each in ascending position (or, for the slot variant, the
 //    cache slots those positions map to).
@@ -61,6 +72,7 @@ constexpr int kSingleMax = 12288;   // rows up to this long run on one CTA each 
 constexpr int kSliceCapMax = 32768; // keys one slice can hold (128 KB of shared memory)
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kMail = 8;  // last-digit bins a slice sends to the later slices
+constexpr uint32_t kLeadCap = 4096;  // candidate keys the leader slice takes (else three cluster rounds)
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 static_assert(kSliceCapMax / kThreads <= 32, "a thread's keys fit one 32-bit mask");
 
@@ -89,6 +101,14 @@ __device__ __forceinline__ void red_add_remote(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void st_remote(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_remote2(uint32_t addr, uint32_t a, uint32_t b) {  // addr 8-byte aligned
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_remote(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ uint4 ld_remote4(uint32_t addr) {  // addr 16-byte aligned
     uint4 v;
     asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -115,6 +135,12 @@ struct __align__(16) Shared {
     uint32_t base[3];                    // keys above / at T before this slice; 1 if a slice sent too many bins
     uint32_t wsum[kWarps];
     uint32_t pick[3];                    // digit, keys above it, keys in it
+    // leader path (slice 0 resolves the rest of T from the first digit's bin)
+    uint32_t gt0[kMaxCluster];           // leader: keys above the first digit's bin, per slice
+    uint32_t gtc[kMaxCluster];           // leader: candidates above T, per slice
+    uint32_t eqc[kMaxCluster];           // leader: candidates equal to T, per slice
+    uint32_t ncand;                      // leader: candidates received
+    uint32_t lead[4];                    // from the leader: T, kr, keys above / at T before this slice
 };
 
 // Exclusive prefix sum over the block in thread order; *total gets the sum.
@@ -235,6 +261,7 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
         for (int b = tid; b < nb; b += kThreads) {
             const uint32_t v = S.hloc[b];
             if (v) {
+                S.hloc[b] = 0u;  // the leader's rounds start from a zero histogram
                 red_add_remote(map_rank(&S.htot[r][b], (uint32_t)(b / per_owner)), v);
                 if (last) {
                     const uint32_t slot = atomicAdd(&S.nz, 1u);
@@ -307,6 +334,73 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
     __syncthreads();
 }
 
+// The leader's digit round over its n candidates (radix keys in cand[i].x)
+// whose bits under `mask` equal `prefix`: a histogram of digit (key >> shift)
+// & (nb - 1) in S.hloc (zero on entry and on return), then the digit holding
+// rank kr (counted from the largest) with the keys above it and in it in
+// S.pick.  Only this CTA's barriers are used.
+__device__ __forceinline__ void cand_round(const uint2* cand, int n, uint32_t prefix, uint32_t mask, int shift,
+                                        int nb, uint32_t kr, Shared& S) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t dm = (uint32_t)nb - 1;
+    for (int i = tid; i < n; i += kThreads) {
+        const uint32_t u = cand[i].x;
+        if ((u & mask) == prefix) atomicAdd(&S.hloc[(u >> shift) & dm], 1u);
+    }
+    __syncthreads();
+    // thread tid holds digits b0 .. b0 + bpt - 1, from the largest down in thread order
+    const int bpt = nb / kThreads < 1 ? 1 : nb / kThreads;  // 2 or 1
+    const int b0 = nb - bpt * (tid + 1);
+    uint32_t t0 = 0, t1 = 0;
+    if (b0 >= 0) {
+        t0 = S.hloc[b0];
+        S.hloc[b0] = 0u;
+        if (bpt == 2) {
+            t1 = S.hloc[b0 + 1];
+            S.hloc[b0 + 1] = 0u;
+        }
+    }
+    const uint32_t sum = t0 + t1;
+    const uint32_t wtot = __reduce_add_sync(kFull, sum);
+    if (lane == 0) S.wsum[warp] = wtot;
+    __syncthreads();
+    const uint32_t wv = lane < kWarps ? S.wsum[lane] : 0u;
+    uint32_t wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(kFull, wi, o);
+        if (lane >= o) wi += x;
+    }
+    const uint32_t wbefore = __shfl_sync(kFull, wi - wv, warp);
+    const uint32_t wafter = __shfl_sync(kFull, wi, warp);
+    if (wbefore < kr && wafter >= kr) {  // warp-uniform
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
+        }
+        uint32_t above = wbefore + incl - sum;
+        if (bpt == 2) {  // the higher digit first
+            if (above < kr && above + t1 >= kr) {
+                S.pick[0] = (uint32_t)(b0 + 1);
+                S.pick[1] = above;
+                S.pick[2] = t1;
+            }
+            above += t1;
+        }
+        if (above < kr && above + t0 >= kr) {
+            S.pick[0] = (uint32_t)b0;
+            S.pick[1] = above;
+            S.pick[2] = t0;
+        }
+    }
+    __syncthreads();
+}
+
+// Words of a slice's radix keys in shared memory (a multiple of 4).
+__host__ __device__ constexpr int slice_words(int cap) { return (cap + 4 + 3) & ~3; }
+
 // List entries as positions, or as physical cache slots of the row's request.
 struct SlotMap {
     const int32_t* table;    // [n_req][max_pages] page ids, or null for positions
@@ -322,7 +416,9 @@ template <int CL>
 __global__ void __launch_bounds__(kThreads)
 k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __restrict__ row_lens,
          int64_t stride, int k, int32_t* __restrict__ out, uint32_t* status, int slice_cap, SlotMap sm) {
-    extern __shared__ __align__(16) uint32_t keys_s[];  // slice_cap radix keys (+ 4)
+    // slice_cap radix keys (+ 4); after them, in clusters of more than one
+    // CTA, the leader's (radix key, row position) of every candidate
+    extern __shared__ __align__(16) uint32_t keys_s[];
     __shared__ Shared S;
     const uint32_t c = cluster_ctarank();
     const int row = blockIdx.y;
@@ -376,6 +472,12 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         uint32_t* h = &S.htot[0][0];
         for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
         if (tid < 2 * kMaxCluster) (&S.cnt[0][0])[tid] = 0;
+        if (tid < kMaxCluster) {
+            S.gt0[tid] = 0;
+            S.gtc[tid] = 0;
+            S.eqc[tid] = 0;
+        }
+        if (tid == 0) S.ncand = 0;
     }
     __syncthreads();
     if (!single) cluster_arrive();  // zeroed totals are released; waited on before the first add
@@ -424,25 +526,128 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     const int m4 = (n4 + kThreads - 1) / kThreads;
     const int j0 = tid * m4 < n4 ? tid * m4 : n4;
     const int j1 = j0 + m4 < n4 ? j0 + m4 : n4;
-    uint32_t prefix = 0, mask = 0, kr = (uint32_t)k;
-#pragma unroll 1
-    for (int r = 0; r < 2; ++r) {
-        const int shift = r == 0 ? 21 : 10;
-        digit_round(keys_s, cnt, prefix, mask, shift, 2048, kr, single, r, CL, r == 0, S);
-        prefix |= S.pick[0] << shift;
-        mask |= 0x7FFu << shift;
-        kr -= S.pick[1];
-    }
-    uint32_t above = 0, cmask = 0;
-    digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, false, S, true, c, j0, j1, &above, &cmask);
-    const uint32_t d_last = S.pick[0];
-    const uint32_t T = prefix | d_last;   // the k-th largest radix key of the row
+    uint32_t kr = (uint32_t)k;
+    digit_round(keys_s, cnt, 0u, 0u, 21, 2048, kr, single, 0, CL, true, S);
+    uint32_t prefix = S.pick[0] << 21, mask = 0x7FFu << 21;
     kr -= S.pick[1];
-    const uint32_t gt_total = (uint32_t)k - kr;
+    uint32_t T, gt_total, base_gt = 0, base_eq = 0, above = 0, cmask = 0, d_last = 0;
+    const bool lead = CL > 1 && !single && S.pick[2] <= kLeadCap;  // the same in every slice of the row
+    if (lead) {
+        // The leader is the last slice: a decode row's top keys crowd into its
+        // most recent positions, so most candidates stay in the leader's own
+        // shared memory.
+        constexpr uint32_t kLeader = (uint32_t)CL - 1;
+        uint2* cand = reinterpret_cast<uint2*>(keys_s + slice_words(slice_cap));
+        // ---- leader path: the keys in the first digit's threshold bin (the
+        //      row's candidates) go to the leader, which finds T among them with
+        //      CTA barriers only and sends every slice T and its offsets.
+        //      Each thread scans its own run once: keys above the bin are
+        //      counted, keys in it are marked (bit 4 (j - j0) + q for position
+        //      4 j + q) and sent to the leader as (radix key, row position).
+        const int lane = tid & 31;
+        for (int j = j0; j < j1; ++j) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys_s)[j];
+            const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (4 * j + q < cnt) {
+                    const uint32_t hi = uu[q] & mask;
+                    if (hi == prefix) cmask |= 1u << (4 * (j - j0) + q);
+                    else above += (uint32_t)(hi > prefix);
+                }
+            }
+        }
+        const uint32_t m = (uint32_t)__popc(cmask);
+        uint32_t incl = m;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
+        }
+        uint32_t at = 0;
+        if (lane == 31 && incl) at = atom_add_remote(map_rank(&S.ncand, kLeader), incl);
+        at = __shfl_sync(kFull, at, 31) + incl - m;
+        for (uint32_t b = cmask; b; b &= b - 1, ++at) {
+            const int i = 4 * j0 + (__ffs(b) - 1);
+            if (at < kLeadCap)
+                st_remote2(map_rank(&cand[at], kLeader), keys_s[i], (uint32_t)(start + i));
+        }
+        const uint32_t wa = __reduce_add_sync(kFull, above);
+        if (lane == 0 && wa) red_add_remote(map_rank(&S.gt0[c], kLeader), wa);
+        cluster_arrive();
+        cluster_wait();  // every candidate and count has reached the leader
+        if (c == kLeader) {
+            const int n_c = (int)(S.ncand < kLeadCap ? S.ncand : kLeadCap);
+            cand_round(cand, n_c, prefix, mask, 10, 2048, kr, S);
+            prefix |= S.pick[0] << 10;
+            mask |= 0x7FFu << 10;
+            kr -= S.pick[1];
+            uint32_t t_key;
+            if (S.pick[2] == 1) {
+                // one candidate has the 22-bit prefix: it is T, and the others
+                // compare with T as their 22-bit prefixes do
+                for (int i = tid; i < n_c; i += kThreads) {
+                    const uint2 e = cand[i];
+                    const int sl = (int)(e.y / (uint32_t)slice_cap);
+                    const uint32_t hi = e.x & mask;
+                    if (hi > prefix) {
+                        atomicAdd(&S.gtc[sl], 1u);
+                    } else if (hi == prefix) {
+                        atomicAdd(&S.eqc[sl], 1u);
+                        S.pick[0] = e.x;
+                    }
+                }
+                __syncthreads();
+                t_key = S.pick[0];
+                kr = 1;
+            } else {
+                cand_round(cand, n_c, prefix, mask, 0, 1024, kr, S);
+                t_key = prefix | S.pick[0];
+                kr -= S.pick[1];
+                for (int i = tid; i < n_c; i += kThreads) {
+                    const uint2 e = cand[i];
+                    const int sl = (int)(e.y / (uint32_t)slice_cap);
+                    if (e.x > t_key) atomicAdd(&S.gtc[sl], 1u);
+                    else if (e.x == t_key) atomicAdd(&S.eqc[sl], 1u);
+                }
+                __syncthreads();
+            }
+            if (tid < CL) {
+                uint32_t bg = 0, be = 0;
+                for (int t = 0; t < tid; ++t) {
+                    bg += S.gt0[t] + S.gtc[t];
+                    be += S.eqc[t];
+                }
+                const uint32_t dst4 = map_rank(&S.lead[0], (uint32_t)tid);
+                st_remote(dst4, t_key);
+                st_remote(dst4 + 4, kr);
+                st_remote(dst4 + 8, bg);
+                st_remote(dst4 + 12, be);
+            }
+        }
+        cluster_arrive();
+        cluster_wait();  // T and the offsets have reached every slice
+        T = S.lead[0];
+        kr = S.lead[1];
+        base_gt = S.lead[2];
+        base_eq = S.lead[3];
+        gt_total = (uint32_t)k - kr;
+    } else {
+        // ---- two more cluster rounds (bits 20..10, then 9..0)
+        digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, CL, false, S);
+        prefix |= S.pick[0] << 10;
+        mask |= 0x7FFu << 10;
+        kr -= S.pick[1];
+        digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, false, S, true, c, j0, j1, &above, &cmask);
+        d_last = S.pick[0];
+        T = prefix | d_last;  // the k-th largest radix key of the row
+        kr -= S.pick[1];
+        gt_total = (uint32_t)k - kr;
+    }
 
     // ---- this thread's counts above and at T, packed (above < 2^11, at <=
-    //      slice_cap < 2^16), scanned in thread order; only the keys that match
-    //      the prefix are looked at again --------------------------------------
+    //      slice_cap < 2^16), scanned in thread order; only the marked keys
+    //      are looked at again --------------------------------------------------
     uint32_t gt = above, eq = 0;
     for (uint32_t m = cmask; m; m &= m - 1) {
         const uint32_t u = keys_s[4 * j0 + (__ffs(m) - 1)];
@@ -450,7 +655,7 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         eq += (uint32_t)(u == T);
     }
     const uint32_t mine = (gt << 16) | eq;
-    if (!single && (tid >> 5) == 0) {
+    if (!single && !lead && (tid >> 5) == 0) {
         // Keys above / at T in the slices before this one, from what they sent
         // with the last round (lane t: slice t), unless a slice had more
         // non-zero bins than it could send.
@@ -479,11 +684,10 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     }
     uint32_t total;
     const uint32_t off = block_scan(mine, &total, S);  // its barriers also publish S.base
-    uint32_t base_gt = 0, base_eq = 0;
-    if (!single && !S.base[2]) {
+    if (!single && !lead && !S.base[2]) {
         base_gt = S.base[0];
         base_eq = S.base[1];
-    } else if (!single) {
+    } else if (!single && !lead) {
         // this slice's counts into every later slice (kept apart: a row's ties
         // may outnumber 2^16)
         if (tid > (int)c && tid < CL) {
@@ -497,7 +701,6 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
             base_eq += S.cnt[1][t];
         }
     }
-
     // ---- ordered writes --------------------------------------------------------
     if (mine) {
         uint32_t pg = base_gt + (off >> 16);
@@ -530,7 +733,12 @@ int slice_cap_for(int cl, int64_t max_len) {
     return (int)(per < kSliceCapMax ? per : kSliceCapMax);
 }
 
-constexpr size_t slice_bytes(int cap) { return (size_t)((cap + 4 + 3) & ~3) * 4; }
+// Dynamic shared memory of k_select<CL>: the slice's keys, then (CL > 1)
+// the leader's candidate buffer.
+template <int CL>
+constexpr size_t slice_bytes(int cap) {
+    return (size_t)slice_words(cap) * 4 + (CL > 1 ? (size_t)kLeadCap * sizeof(uint2) : 0);
+}
 
 // Once per device (and host thread: setting the attributes is idempotent):
 // cluster and shared-memory attributes of k_select<CL>.
@@ -544,7 +752,7 @@ cudaError_t configure(int dev) {
         if (err != cudaSuccess) return err;
     }
     err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)slice_bytes(kSliceCapMax));
+                               (int)slice_bytes<CL>(kSliceCapMax));
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(k_select<CL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
@@ -564,7 +772,7 @@ cudaError_t launch_c(const SelectArgs& a) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, (unsigned)a.R, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = slice_bytes(cap);
+    cfg.dynamicSmemBytes = slice_bytes<CL>(cap);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -600,7 +808,7 @@ int max_active_clusters(int cap) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(CL, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = slice_bytes(cap);
+        cfg.dynamicSmemBytes = slice_bytes<CL>(cap);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = CL;

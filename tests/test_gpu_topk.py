@@ -200,6 +200,24 @@ def test_crowded_first_digit(n, placement, c1):
     _check_rows(s[None, :], [n], 2048, got)
 
 
+@pytest.mark.parametrize("placement", ["spread", "first_keys"])
+@pytest.mark.parametrize("c1", [4096, 4097])
+def test_leader_capacity_boundary(placement, c1):
+    """A split row whose first digit's threshold bin holds exactly the 4,096
+    candidates the leader slice takes, or one more (then the two further
+    cluster rounds run instead); spread over the row or crowded into its
+    first slices, far from the leader (the last slice)."""
+    n = 131072
+    rng = np.random.default_rng(c1 + len(placement))
+    s = rng.uniform(0.1, 0.9, n).astype(np.float32)
+    pos = rng.choice(n, 1000 + c1, replace=False) if placement == "spread" else rng.permutation(1000 + c1)
+    s[pos[:1000]] = rng.uniform(2.0, 4.0, 1000).astype(np.float32)
+    s[pos[1000:]] = (1.0 + 0.2499 * rng.random(c1)).astype(np.float32)
+    got, st = gpu_topk(s[None, :], [n], 2048)
+    assert st == 0
+    _check_rows(s[None, :], [n], 2048, got)
+
+
 @pytest.mark.parametrize("n", [30000, 131072])
 @pytest.mark.parametrize("distinct", [1, 3, 8, 9, 40, 1024])
 def test_last_digit_bins(n, distinct):
