@@ -566,8 +566,8 @@ def main():
         "trials": {"n": len(trial_secs), "steps_each": args.steps,
                    "per_step_us": [round(x * 1e6, 3) for x in trial_secs],
                    "mean_us": float(np.mean(trial_secs)) * 1e6, "statistic": "median"},
-        "gpu_launches": 2 * args.steps,           # per timed trial (scoring + selection per step)
-        "gpu_launches_all_trials": 2 * args.steps * len(trial_secs),
+        "gpu_launches": 3 * args.steps,           # per timed trial (query prep, scoring, selection per step)
+        "gpu_launches_all_trials": 3 * args.steps * len(trial_secs),
         "clocks": clocks,
     }
     if not args.no_8k:

@@ -299,7 +299,7 @@ idx_status idx_topk(const float* scores, int64_t score_stride, const int32_t* ro
     if (score_stride < 4 || score_stride % 4 != 0 || !aligned(scores, 16)) return IDX_ERR_ALIGN;
     uint32_t* status = nullptr;
     if (workspace) {
-        if (ws_bytes < ws_layout(R, score_stride, 0).end) return IDX_ERR_WORKSPACE;
+        if (ws_bytes < ws_layout(R, score_stride, 0, 0).end) return IDX_ERR_WORKSPACE;
         status = static_cast<uint32_t*>(workspace);
     }
     DeviceInfo dev;
@@ -518,7 +518,7 @@ idx_status idx_score_noalloc(int qtype, const void* q, const float* head_w, cons
     char* scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != IDX_OK) return st;
-    const WsLayout L = ws_layout(R, score_stride, 0);
+    const WsLayout L = ws_layout(R, score_stride, 0, 0);  // the status word only: the query is split in the kernel
     if (L.end > kNoallocScratchBytes) return IDX_ERR_WORKSPACE;
     ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                 R, scores, score_stride, score_stride, scratch, L, static_cast<cudaStream_t>(stream), dev.num_sms};

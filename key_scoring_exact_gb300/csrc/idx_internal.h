@@ -24,9 +24,12 @@ constexpr int kSelectThreads = 256;
 constexpr uint32_t kStatusBounds = 1u;   // block-table id outside the pool / row too long
 constexpr uint32_t kStatusTimeout = 2u;  // a bounded wait gave up
 
-// Workspace layout: the status word, then (optionally) an f32 score matrix.
+// Workspace layout: the status word; the rows' prepared query operands (hi
+// and lo E4M3 terms of 8 KB and 64 f32 head weights a row, for the scoring
+// calls); then (optionally) an f32 score matrix.
 struct WsLayout {
     size_t status;   // uint32 status word
+    size_t qop;      // [R] prepared query operands (0: none)
     size_t scores;   // f32 [R][score_stride] (optional)
     size_t end;
     int64_t score_stride;
@@ -34,13 +37,16 @@ struct WsLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int R, int64_t max_len, int with_scores) {
+constexpr size_t kQopRowBytes = 2 * 8192 + 64 * 4;
+
+inline WsLayout ws_layout(int R, int64_t max_len, int with_scores, int with_qop = 1) {
     WsLayout L{};
     L.status = 0;
     L.score_stride = (max_len + 3) / 4 * 4;
     if (L.score_stride < 4) L.score_stride = 4;
-    L.scores = 1024;
-    L.end = with_scores ? align_up(L.scores + sizeof(float) * (size_t)R * (size_t)L.score_stride, 1024) : 1024;
+    L.qop = with_qop ? 1024 : 0;
+    L.scores = with_qop ? align_up(1024 + kQopRowBytes * (size_t)R, 1024) : 1024;
+    L.end = with_scores ? align_up(L.scores + sizeof(float) * (size_t)R * (size_t)L.score_stride, 1024) : L.scores;
     return L;
 }
 

@@ -70,6 +70,7 @@ constexpr int kEpiWarps = 16;                              // 4 rows x 4 TMEM la
 constexpr int kScoreThreads = 64 + kEpiWarps * 32;         // 576
 constexpr uint32_t kQRows = kGroupRows * kHeads;           // 256
 constexpr uint32_t kQPartBytes = kQRows * kDim;            // 32 KB
+constexpr uint32_t kQRowBytes = kHeads * kDim;             // 8 KB: one row's operand term
 constexpr uint32_t kPageKeyBytes = kPage * kDim;           // 8 KB
 constexpr uint32_t kPageScaleBytes = kPage * 4;            // 256 B
 constexpr uint32_t kStageBytes = kTileKeys * kDim;         // 16 KB
@@ -87,7 +88,7 @@ constexpr uint32_t kOffPlan = kOffWq + 2 * kQRows * 4;
 // plan: item[kMaxRows+1], req, r0, nr, len [kMaxRows] each, row_len[kMaxRows], gid[kMaxRows]
 constexpr uint32_t kPlanInts = (kMaxRows + 1) + 4 * kMaxRows + 2 * kMaxRows;
 constexpr uint32_t kOffBars = ((kOffPlan + kPlanInts * 4) + 7) & ~7u;
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 2;
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 4;
 constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -109,6 +110,7 @@ struct ScoreParams {
     float* scores;
     int64_t score_stride;
     uint32_t* status;
+    uint8_t* qop;            // the rows' prepared operands (k_qprep), or null: split in the kernel
     uint64_t wait_ns;        // wall-time limit of every role's waits (kWaitTimeoutNs in normal use)
     int drop_query_handoff;  // test only: the epilogue never signals the query operand
 };
@@ -143,8 +145,8 @@ __device__ void build_plan(const ScoreParams& p, const PlanSmem& pl, int* n_grou
     for (int base = 0; base < R; base += 32) {
         const int r = base + lane;
         const bool valid = r < R;
-        const int req = valid ? p.row_req[r] : -1;
-        int len = valid ? p.seq_lens[r] : 0;
+        const int req = valid ? __ldcg(p.row_req + r) : -1;  // through L2 (read before the grid wait)
+        int len = valid ? __ldcg(p.seq_lens + r) : 0;
         if (valid) {
             if (len < 0 || (int64_t)len > p.len_cap || req < 0) bad = true;
             len = len < 0 ? 0 : ((int64_t)len > p.len_cap ? (int)p.len_cap : len);
@@ -207,17 +209,22 @@ __device__ __forceinline__ uint16_t to_e4m3_pair(float a, float b) {
     return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-__device__ __forceinline__ float e4m3_to_float(uint16_t codes, int which) {
-    __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
-    __half_raw h;
-    h.x = which ? h2.y : h2.x;
-    return __half2float(__half(h));
-}
-
 // 2 ReLU(x) = x + |x|: one add (the absolute value is an operand modifier)
 // on the FMA pipe instead of a max on the half-rate ALU pipe; exact, and a NaN
 // passes through as it does in the definition's ReLU.
 __device__ __forceinline__ float relu2(float x) { return __fadd_rn(x, fabsf(x)); }
+
+// x rounded to the nearest E4M3 value, ties to even, as an f32, for |x| < 448
+// (the value whose code cvt.rn.satfinite.e4m3x2.f32 gives): in E4M3's
+// normal range (|x| >= 2^-6) the f32 mantissa is rounded to 3 bits in the
+// integer unit; below it to a multiple of 2^-9 (E4M3's subnormal spacing) by
+// adding and subtracting 1.5 * 2^14.
+__device__ __forceinline__ float round_e4m3(float x) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t rn = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
+    const float sub = __fsub_rn(__fadd_rn(x, 24576.0f), 24576.0f);
+    return fabsf(x) >= 0.015625f ? __uint_as_float(rn) : sub;
+}
 
 __device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]: exact 2^e
     return __int_as_float((e + 127) << 23);
@@ -229,8 +236,44 @@ __device__ __forceinline__ uint32_t swz_off(int n, int lane) {
     return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((((lane >> 2) ^ (n & 7)) & 7) << 4) + ((lane & 3) << 2));
 }
 
+// One (row, head) vector of a bf16 query split exactly into hi + lo E4M3
+// terms after scaling by 2^ex (warp-collective: lane l holds elements 4l ..
+// 4l + 3 as two packed bf16 pairs in `raw`).  Returns the lane's four hi and
+// four lo codes and 2^-ex, the factor folded into the head weight.
+struct PairSplit {
+    uint32_t hi, lo;
+    float inv_scale;
+};
+__device__ __forceinline__ PairSplit split_pair(uint2 raw) {
+    float x[4];
+    x[0] = __uint_as_float(raw.x << 16);
+    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(raw.y << 16);
+    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    // Largest exponent field of the 128 elements (one warp reduction); the
+    // largest element lies in [2^(E-127), 2^(E-126)).
+    const uint32_t e01 = max((raw.x >> 7) & 0xFFu, (raw.x >> 23) & 0xFFu);
+    const uint32_t e23 = max((raw.y >> 7) & 0xFFu, (raw.y >> 23) & 0xFFu);
+    const int emax = (int)__reduce_max_sync(0xFFFFFFFFu, max(e01, e23));
+    // 2^ex brings the largest element into [128, 256) (<= 448).
+    const int ex = max(-126, min(126, 134 - emax));
+    const float sc = pow2f(ex);
+    float xs[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        xs[i] = x[i] * sc;
+        lo[i] = __fsub_rn(xs[i], round_e4m3(xs[i]));
+    }
+    PairSplit r;
+    r.hi = (uint32_t)to_e4m3_pair(xs[0], xs[1]) | ((uint32_t)to_e4m3_pair(xs[2], xs[3]) << 16);
+    r.lo = (uint32_t)to_e4m3_pair(lo[0], lo[1]) | ((uint32_t)to_e4m3_pair(lo[2], lo[3]) << 16);
+    r.inv_scale = pow2f(-ex);
+    return r;
+}
+
 // The epilogue warps split the query of a group (rows r0 .. r0+nr-1) into
-// the hi / lo operand buffers and write w' for each (row, head).
+// the hi / lo operand buffers and write w' for each (row, head) (launches
+// without a prepared operand: idx_score_noalloc).
 __device__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t* q_hi, uint8_t* q_lo,
                                   float* wq, int e, int lane) {
     const int pairs = nr * kHeads;
@@ -293,35 +336,70 @@ __device__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t*
         for (int b = 0; b < kBatch; ++b) {
             const int pp = p0 + b * kEpiWarps;
             if (pp >= pairs) break;  // warp-uniform
-            float x[4];
-            x[0] = __uint_as_float(raw[b].x << 16);
-            x[1] = __uint_as_float(raw[b].x & 0xFFFF0000u);
-            x[2] = __uint_as_float(raw[b].y << 16);
-            x[3] = __uint_as_float(raw[b].y & 0xFFFF0000u);
-            // Largest exponent field of the 128 elements (one warp reduction);
-            // the largest element lies in [2^(E-127), 2^(E-126)).
-            const uint32_t e01 = max((raw[b].x >> 7) & 0xFFu, (raw[b].x >> 23) & 0xFFu);
-            const uint32_t e23 = max((raw[b].y >> 7) & 0xFFu, (raw[b].y >> 23) & 0xFFu);
-            const int emax = (int)__reduce_max_sync(0xFFFFFFFFu, max(e01, e23));
-            // 2^ex brings the largest element into [128, 256) (<= 448).
-            const int ex = max(-126, min(126, 134 - emax));
-            const float sc = pow2f(ex);
-            float xs[4], lo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) xs[i] = x[i] * sc;
-            const uint16_t h01 = to_e4m3_pair(xs[0], xs[1]);
-            const uint16_t h23 = to_e4m3_pair(xs[2], xs[3]);
-            lo[0] = __fsub_rn(xs[0], e4m3_to_float(h01, 0));
-            lo[1] = __fsub_rn(xs[1], e4m3_to_float(h01, 1));
-            lo[2] = __fsub_rn(xs[2], e4m3_to_float(h23, 0));
-            lo[3] = __fsub_rn(xs[3], e4m3_to_float(h23, 1));
-            const uint16_t l01 = to_e4m3_pair(lo[0], lo[1]);
-            const uint16_t l23 = to_e4m3_pair(lo[2], lo[3]);
+            const PairSplit sp = split_pair(raw[b]);
             const uint32_t off = swz_off(pp, lane);
-            *reinterpret_cast<uint32_t*>(q_hi + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
-            *reinterpret_cast<uint32_t*>(q_lo + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
-            if (lane == 0) wq[pp] = wv[b] * pow2f(-ex);
+            *reinterpret_cast<uint32_t*>(q_hi + off) = sp.hi;
+            *reinterpret_cast<uint32_t*>(q_lo + off) = sp.lo;
+            if (lane == 0) wq[pp] = wv[b] * sp.inv_scale;
         }
+    }
+}
+
+// ---- k_qprep: the query operand of every row, once per call ----------------
+//
+// Row r's operand in the workspace, in the shared-memory layout the scoring
+// copies verbatim (K-major, 128-byte swizzle, 1024-byte atoms of 8 heads):
+//   hi [R][8192 B] at qop, lo [R][8192 B] at qop + R * 8192 (bf16 query only),
+//   w' [R][64] f32 at qop + 2 * R * 8192.
+// A group of rows r0 .. r0 + nr - 1 is then one contiguous run of each.
+constexpr int kQprepThreads = 256;
+constexpr int kQprepPairsPerWarp = 1;
+
+__global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
+    // Wait for the kernel before this one, then let the scoring launch (a
+    // programmatic dependent) start: every input written before this call is
+    // then complete, so the scoring may read the inputs other than this
+    // kernel's operands before its own grid wait.
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int warp_g = blockIdx.x * (kQprepThreads / 32) + (threadIdx.x >> 5);
+    const int pairs = p.R * kHeads;
+    uint8_t* hi = p.qop;
+    uint8_t* lo = p.qop + (int64_t)p.R * kQRowBytes;
+    float* wq = reinterpret_cast<float*>(p.qop + 2 * (int64_t)p.R * kQRowBytes);
+    uint2 raw[kQprepPairsPerWarp];
+    float wv[kQprepPairsPerWarp];
+#pragma unroll
+    for (int b = 0; b < kQprepPairsPerWarp; ++b) {
+        const int pp = warp_g * kQprepPairsPerWarp + b;
+        raw[b] = make_uint2(0u, 0u);
+        wv[b] = 0.0f;
+        if (pp < pairs) {
+            if (p.qtype == IDX_Q_E4M3) raw[b].x = reinterpret_cast<const uint32_t*>(p.q)[(int64_t)pp * 32 + lane];
+            else raw[b] = reinterpret_cast<const uint2*>(p.q)[(int64_t)pp * 32 + lane];
+            wv[b] = p.head_w[pp];
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kQprepPairsPerWarp; ++b) {
+        const int pp = warp_g * kQprepPairsPerWarp + b;
+        if (pp >= pairs) break;  // warp-uniform
+        const int64_t off = (int64_t)(pp / kHeads) * kQRowBytes + swz_off(pp % kHeads, lane);
+        float w_out = wv[b];
+        if (p.qtype == IDX_Q_BF16) {
+            const PairSplit sp = split_pair(raw[b]);
+            *reinterpret_cast<uint32_t*>(hi + off) = sp.hi;
+            *reinterpret_cast<uint32_t*>(lo + off) = sp.lo;
+            w_out = wv[b] * sp.inv_scale;
+        } else if (p.qtype == IDX_Q_BF16_FP8) {
+            float scale;
+            *reinterpret_cast<uint32_t*>(hi + off) = quantize_head_lane(raw[b], &scale);
+            w_out = __fmul_rn(wv[b], scale);
+        } else {
+            *reinterpret_cast<uint32_t*>(hi + off) = raw[b].x;
+        }
+        if (lane == 0) wq[pp] = w_out;
     }
 }
 
@@ -364,6 +442,8 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
     uint64_t* tempty = tfull + 2;             // [2] accumulator drained
     uint64_t* qfull = tempty + 2;             // the group's query operand written
     uint64_t* drain = qfull + 1;              // final MMA completion
+    uint64_t* qcopy = drain + 1;              // the group's prepared operand copied in
+    uint64_t* grp_ready = qcopy + 1;          // every epilogue warp is done with the previous group
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* counts = reinterpret_cast<int*>(smem + kOffMisc + 8);  // n_groups, n_items
@@ -389,6 +469,8 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         }
         mbar_init(qfull, kEpiWarps);
         mbar_init(drain, 1);
+        mbar_init(qcopy, 1);
+        mbar_init(grp_ready, kEpiWarps);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&keys_map);
@@ -398,9 +480,13 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         tmem_relinquish();
     }
     // Launched as a programmatic dependent of the kernel before it on the
-    // stream: wait for that grid to finish before reading an input or writing
-    // a score (only barriers and TMEM are set up before this point).
-    pdl_wait();
+    // stream.  With a prepared operand that kernel is k_qprep, which lets this
+    // grid launch only once every kernel before it has completed: the plan
+    // inputs, block table and keys are read at once (through L2), and the
+    // MMA warp waits for k_qprep to finish (griddepcontrol.wait) before
+    // copying the operand.  Without one, wait for the kernel before before
+    // reading an input or writing a score.
+    if (!p.qop) pdl_wait();
     if (warp == 0) build_plan(p, pl, &counts[0], &counts[1]);
     tc_fence_before_sync();
     __syncthreads();
@@ -431,7 +517,7 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
             if (lane < 2 * nb) {
                 const int pidx = 2 * t0 + lane;
                 if (pidx < npages) {
-                    const int v = p.block_table[(int64_t)req * p.max_pages + pidx];
+                    const int v = __ldcg(p.block_table + (int64_t)req * p.max_pages + pidx);
                     if (v < 0 || (int64_t)v >= p.pool_pages) record_status(p.status, kStatusBounds);
                     else id = v;
                 }
@@ -480,12 +566,33 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
             int g = find_group(pl, n_groups, it0), qi = 0;
             int gend = -1;  // first work item past the current group
             uint32_t idesc = 0;
+            bool copy_pending = false;
             for (int it = it0, li = 0; it < it1; ++it, ++li) {
                 if (it >= gend) {
                     while (g + 1 < n_groups && it >= pl.item[g + 1]) ++g;
                     gend = pl.item[g + 1];
-                    // the epilogue has written this group's query operand
-                    if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) break;
+                    if (p.qop) {
+                        // Copy the group's prepared operand and w' in, once every
+                        // epilogue warp is done with the previous group (so its
+                        // MMAs have completed and its w' is no longer read).
+                        if (qi > 0 && !bounded_wait(grp_ready, (qi - 1) & 1, abort_flag, p.wait_ns)) break;
+                        if (qi == 0) pdl_wait();  // k_qprep has written every operand
+                        if (!p.drop_query_handoff) {
+                            const int r0g = pl.r0[g], nrg = pl.nr[g];
+                            const bool two = p.qtype == IDX_Q_BF16;
+                            const uint32_t term = (uint32_t)nrg * kQRowBytes;
+                            mbar_arrive_expect_tx(qcopy, term * (two ? 2u : 1u) + (uint32_t)nrg * kHeads * 4u);
+                            bulk_load(q_hi, p.qop + (int64_t)r0g * kQRowBytes, term, qcopy);
+                            if (two) bulk_load(q_lo, p.qop + ((int64_t)p.R + r0g) * kQRowBytes, term, qcopy);
+                            bulk_load(wq_s, p.qop + 2 * (int64_t)p.R * kQRowBytes + (int64_t)r0g * kHeads * 4,
+                                      (uint32_t)nrg * kHeads * 4u, qcopy);
+                            copy_pending = true;
+                        }
+                        if (!bounded_wait(qcopy, qi & 1, abort_flag, p.wait_ns)) break;
+                        copy_pending = false;
+                    } else if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) {
+                        break;  // the epilogue has written this group's query operand
+                    }
                     tc_fence_after_sync();
                     idesc = idesc_e4m3_f32(128, (uint32_t)pl.nr[g] * kHeads);
                     ++qi;
@@ -502,10 +609,12 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 }
                 mma_commit(&tfull[li & 1]);
             }
-            // Every MMA issued here must finish before TMEM is released.
+            // Every MMA issued here must finish before TMEM is released, and an
+            // operand copy in flight before the CTA leaves.
             int dummy = 0;
             mma_commit(drain);
             bounded_wait(drain, 0, &dummy);
+            if (copy_pending) bounded_wait(qcopy, (qi & 1), &dummy);
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -528,13 +637,25 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
                 r0 = pl.r0[g];
                 nr = pl.nr[g];
                 rlen = rr < nr ? pl.row_len[r0 + rr] : 0;
-                float* wbuf = wq_s + (qi & 1) * kQRows;
-                split_group_query(p, r0, nr, q_hi, q_lo, wbuf, e, lane);
-                fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's operand reads
-                __syncwarp();
-                if (lane == 0 && !p.drop_query_handoff) mbar_arrive(qfull);
-                if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) break;  // every warp's w' is written
-                w = wbuf + rr * kHeads;
+                if (p.qop) {
+                    // the MMA warp copies the prepared operand and w' in once
+                    // every epilogue warp is done with the previous group
+                    if (qi > 0) {
+                        fence_proxy_async_smem();  // this warp's reads of w' -> the copy's writes
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(grp_ready);
+                    }
+                    if (!bounded_wait(qcopy, qi & 1, abort_flag, p.wait_ns)) break;
+                    w = wq_s + rr * kHeads;
+                } else {
+                    float* wbuf = wq_s + (qi & 1) * kQRows;
+                    split_group_query(p, r0, nr, q_hi, q_lo, wbuf, e, lane);
+                    fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's operand reads
+                    __syncwarp();
+                    if (lane == 0 && !p.drop_query_handoff) mbar_arrive(qfull);
+                    if (!bounded_wait(qfull, qi & 1, abort_flag, p.wait_ns)) break;  // every warp's w' is written
+                    w = wbuf + rr * kHeads;
+                }
                 if constexpr (kRegW) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -671,6 +792,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.scores = a.scores;
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
+    p.qop = a.L.qop ? reinterpret_cast<uint8_t*>(a.ws + a.L.qop) : nullptr;
     const WaitTestHook hook = wait_test_hook();
     p.wait_ns = hook.wait_ns ? hook.wait_ns : kWaitTimeoutNs;
     p.drop_query_handoff = hook.drop_query_handoff;
@@ -693,6 +815,19 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.qop) {
+        // the rows' operands first, as the scoring's predecessor on the stream
+        const int pairs = p.R * kHeads;
+        const int per_cta = (kQprepThreads / 32) * kQprepPairsPerWarp;
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3((unsigned)((pairs + per_cta - 1) / per_cta), 1, 1);
+        qc.blockDim = dim3(kQprepThreads, 1, 1);
+        qc.stream = a.stream;
+        qc.attrs = attr;
+        qc.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&qc, k_qprep, p);
+        if (e != cudaSuccess) return e;
+    }
     return reg_w ? cudaLaunchKernelEx(&cfg, k_score<true>, keys_map, p)
                  : cudaLaunchKernelEx(&cfg, k_score<false>, keys_map, p);
 }
