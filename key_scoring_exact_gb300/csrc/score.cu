@@ -273,8 +273,10 @@ __device__ __forceinline__ PairSplit split_pair(uint2 raw) {
 
 // The epilogue warps split the query of a group (rows r0 .. r0+nr-1) into
 // the hi / lo operand buffers and write w' for each (row, head) (launches
-// without a prepared operand: idx_score_noalloc).
-__device__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t* q_hi, uint8_t* q_lo,
+// without a prepared operand: idx_score_noalloc).  Not inlined: it is off the
+// usual path, and inlined it would push the tile loop's registers past the
+// cap.
+__device__ __noinline__ void split_group_query(const ScoreParams& p, int r0, int nr, uint8_t* q_hi, uint8_t* q_lo,
                                   float* wq, int e, int lane) {
     const int pairs = nr * kHeads;
     if (p.qtype != IDX_Q_BF16) {
