@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, help="workload configuration 1..5")
+    ap.add_argument("--workload", default=None, help="an extra workload instead of --config (chain8)")
+    ap.add_argument("--no-chain8", action="store_true", help="skip the 8-row chain measurement")
     ap.add_argument("--copies", type=int, default=COPIES)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -504,7 +506,7 @@ def config_desc(w, args):
 def main():
     args = parse()
     from key_scoring_exact_gb300 import workloads as W
-    w = W.make_config(args.config)
+    w = W.make_extra(args.workload) if args.workload else W.make_config(args.config)
     args.copies = copies_for(w, args.copies)   # the same rotation (and config line) in both arms
     if args.impl == "reference":
         reference_main(args, w)
@@ -605,6 +607,21 @@ def main():
                                 "scoring_gbs_of_keys": wb.unique_key_bytes() / tb_score / 1e9,
                                 "keys_per_s": wb.row_keys() / secb}
         del stb
+    if not args.no_chain8 and not args.workload:
+        # an MTP chain of 8 verify rows: two groups of four rows whose key
+        # reads run on different CTAs at the same time (the second from L2)
+        wc = W.make_extra("chain8")
+        stc = Step(wc, copies_for(wc, 2), dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                stc.fused(i, stream)
+            secc, _ = time_graph_steps(stc, min(args.steps, 1024), stream, None)
+            tc_score, tc_select = per_kernel_times(stc, min(args.steps, 256), stream)
+        line["also_chain8"] = {"workload": wc.recipe, "us": secc * 1e6, "scoring_us": tc_score * 1e6,
+                               "selection_us": tc_select * 1e6, "keys_per_s": wc.row_keys() / secc,
+                               "dram_read_bytes_per_scoring_launch": ncu_traffic("k_score_chain8", "score.cu"),
+                               "unique_key_bytes": wc.unique_key_bytes()}
+        del stc
     if not args.no_fp8q and not w.q_is_e4m3:
         # the same workload with the query quantised to E4M3 on the device (one
         # E4M3 term: half the MMAs); scores are those of the quantised query

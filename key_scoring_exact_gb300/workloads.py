@@ -203,6 +203,25 @@ CONFIG_RECIPES = {
 }
 
 
+# Workloads beside the five configurations (measured by the benchmark as
+# extras): an MTP draft chain of 8 verify rows, whose rows form two groups of
+# four that score the same keys.
+EXTRA_RECIPES = {
+    "chain8": "1 request, 8 verify rows seeing 131,065..131,072 keys; random keys, scales "
+              "U(0.5,2), shuffled pages; bf16 q; k=2048",
+}
+
+
+def make_extra(name: str, seed: int = 6, q_is_e4m3: bool = False) -> Workload:
+    """One of EXTRA_RECIPES."""
+    if name == "chain8":
+        w = make_workload([chain(131072, 8)], "random", seed, q_is_e4m3, name="chain8")
+    else:
+        raise ValueError("extra workloads: %s" % ", ".join(EXTRA_RECIPES))
+    w.recipe = EXTRA_RECIPES[name]
+    return w
+
+
 def make_config(idx: int, seed: int | None = None, q_is_e4m3: bool = False) -> Workload:
     """Configuration idx (1..5) with its fixed seed (= idx unless given)."""
     s = idx if seed is None else seed

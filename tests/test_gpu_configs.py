@@ -55,6 +55,18 @@ def test_config5_sampled():
     _lists_exact(w, s, got)
 
 
+def test_chain_of_eight_rows():
+    """An MTP draft chain of 8 verify rows at 131K keys (two groups of four
+    rows scoring the same keys): every score within 1e-4, every list exact."""
+    w = W.make_extra("chain8")
+    s, got, st = gpu_fused(w)
+    assert st == 0
+    ref = oracle.scores(problem(w))
+    errs = checks.score_errors(s, ref, w.seq_lens.tolist())
+    assert max(errs) <= checks.SCORE_TOL, errs
+    _lists_exact(w, s, got)
+
+
 def test_scores_in_workspace():
     w = W.make_config(1)
     s1, got1, st1 = gpu_fused(w)
