@@ -427,6 +427,19 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     // up on the SMs this launch leaves free; it waits for this grid to finish
     // before it reads or writes anything in global memory.
     pdl_launch_dependents();
+    // Shared-memory set-up, which reads no global memory, overlaps the wait.
+    for (int i = tid; i < kBinsMax; i += kThreads) S.hloc[i] = 0;
+    {
+        uint32_t* h = &S.htot[0][0];
+        for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
+    }
+    if (tid < 2 * kMaxCluster) (&S.cnt[0][0])[tid] = 0;
+    if (tid < kMaxCluster) {
+        S.gt0[tid] = 0;
+        S.gtc[tid] = 0;
+        S.eqc[tid] = 0;
+    }
+    if (tid == 0) S.ncand = 0;
     // This launch is itself a programmatic dependent of the kernel before it
     // (the scoring): wait for that grid before reading a score.
     pdl_wait();
@@ -467,19 +480,7 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     if (single && c != 0) return;   // one CTA serves the row; no cluster barrier is used
     const int cnt = (int)(start < n ? (n - start < slice_cap ? n - start : slice_cap) : 0);
 
-    for (int i = tid; i < kBinsMax; i += kThreads) S.hloc[i] = 0;
-    if (!single) {
-        uint32_t* h = &S.htot[0][0];
-        for (int i = tid; i < 3 * kBinsMax; i += kThreads) h[i] = 0;
-        if (tid < 2 * kMaxCluster) (&S.cnt[0][0])[tid] = 0;
-        if (tid < kMaxCluster) {
-            S.gt0[tid] = 0;
-            S.gtc[tid] = 0;
-            S.eqc[tid] = 0;
-        }
-        if (tid == 0) S.ncand = 0;
-    }
-    __syncthreads();
+    __syncthreads();  // the shared memory zeroed before the grid wait is visible to every thread
     if (!single) cluster_arrive();  // zeroed totals are released; waited on before the first add
 
     // ---- radix keys into shared memory and the first round's histogram
