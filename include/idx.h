@@ -169,6 +169,39 @@ idx_status idx_score_topk_slots(int qtype, const void *q, const float *head_w,
                                 void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_score_topk_tagged -- idx_score_topk whose lists are written as tagged
+ * pairs, the hand-off of "sgl-amd-mono-upstream PR 11" (GLM-5.3-Flash
+ * monokernel hand-offs), section "3. The selected tokens are tagged pairs": a
+ * consumer polls the list entries themselves for the launch's tag instead of a
+ * separate ready flag written after them.  Entry j of row r is
+ *
+ *     pairs[r][j] = ((uint64_t)tag << 32) | (uint32_t)entry
+ *
+ * i.e. the int32 words {entry, tag} in that order in memory, stored with one
+ * 8-byte store, so a reader that finds `tag` in a pair (with an 8-byte load)
+ * finds this launch's entry beside it.  entry is the list entry of
+ * idx_score_topk (a logical position), or with slots != 0 that of
+ * idx_score_topk_slots (a physical cache slot); -1 padding is stored as
+ * {-1, tag}, so a short row is complete once all k pairs carry the tag.  The
+ * caller picks the tag (a step counter, say) and must not reuse the tag of a
+ * launch whose pairs a reader might still mistake for this one's.
+ *
+ *  tag          32-bit launch tag
+ *  slots        0: positions, else physical cache slots
+ *  pairs        [R][k] int64 out, 8-byte aligned (else IDX_ERR_ALIGN)
+ *
+ * The other arguments, the list order and the errors are those of
+ * idx_score_topk.
+ */
+idx_status idx_score_topk_tagged(int qtype, const void *q, const float *head_w,
+                                 const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                                 const int32_t *block_table, int max_pages,
+                                 const int32_t *seq_lens, const int32_t *row_req, int R,
+                                 int64_t max_len, int k, uint32_t tag, int slots, int64_t *pairs,
+                                 float *scores, int64_t score_stride,
+                                 void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_quantize_query -- the FP8 (E4M3) query of a bf16 index query, one scale
  * per (row, head), as IDX_Q_BF16_FP8 scoring uses it.  The recipe is the
  * per-token FP8 quantisation of "[Perf] [MI355X] minimax_m31" (section

@@ -22,7 +22,8 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
 
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
-           "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots")
+           "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots",
+           "idx_score_topk_tagged")
 DIAG_EXPORTS = ("idx_probe_fp8_mma", "idx_test_set_wait_limit")   # include/idx_diag.h
 
 _lib = None
@@ -63,6 +64,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_score_topk.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
     lib.idx_score_topk_slots.restype = i32
     lib.idx_score_topk_slots.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
+    lib.idx_score_topk_tagged.restype = i32
+    lib.idx_score_topk_tagged.argtypes = score_common + [i64, i32, ctypes.c_uint32, i32, p, p, i64, p, sz, p]
     lib.idx_check_status.restype = i32
     lib.idx_check_status.argtypes = [p, p]
     lib.idx_status_str.restype = ctypes.c_char_p
@@ -218,6 +221,21 @@ def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_
     st = fn(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
             stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "idx_score_topk_slots" if slots else "idx_score_topk")
+
+
+def score_topk_tagged(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, tag, pairs,
+                      workspace, scores=None, stream=None, quantize_q=False, slots=False):
+    """idx_score_topk_tagged: as score_topk, the lists written into `pairs`
+    ([R, k] int64) as tagged pairs (tag << 32) | uint32(entry)."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
+    if pairs.shape != (q.shape[0], k):
+        raise ValueError("pairs must be [R, k]")
+    sp = _dev(scores, "scores", torch.float32) if scores is not None else None
+    stride = int(scores.shape[1]) if scores is not None else 0
+    st = load().idx_score_topk_tagged(*args, int(max_len), int(k), int(tag) & 0xFFFFFFFF, 1 if slots else 0,
+                                      _dev(pairs, "pairs", torch.int64), sp, stride,
+                                      _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "idx_score_topk_tagged")
 
 
 def host_workspace_bytes(R: int, max_len: int, k: int, n_req: int, max_pages: int) -> int:

@@ -216,16 +216,19 @@ const void* mapped(const void* host) {
 }
 }  // namespace
 
-// The fused call; with `slots` the lists hold physical cache slots.
+// The fused call; with `slots` the lists hold physical cache slots, with
+// `pairs` they are written as tagged pairs (indices unused).
 static idx_status score_topk_impl(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
                           const float* k_scale, int64_t pool_pages, const int32_t* block_table, int max_pages,
                           const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
-                          size_t ws_bytes, void* stream, bool slots) {
+                          size_t ws_bytes, void* stream, bool slots, long long* pairs = nullptr,
+                          uint32_t tag = 0) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
-    if (!indices || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
+    if ((!indices && !pairs) || k < 1 || k > IDX_MAX_K || max_len < 1) return IDX_ERR_ARG;
+    if (pairs && !aligned(pairs, 8)) return IDX_ERR_ALIGN;
     const int64_t cap = (int64_t)max_pages * kPage;
     if (max_len > cap) max_len = cap;
     if (max_len > kSelectMaxLen) return IDX_ERR_ARG;
@@ -255,6 +258,8 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
         sel.slot_row_req = row_req;
         sel.slot_max_pages = max_pages;
     }
+    sel.pairs = pairs;
+    sel.tag = tag;
     return to_status(launch_select(sel));
 }
 
@@ -327,6 +332,17 @@ idx_status idx_score_topk_slots(int qtype, const void* q, const float* head_w, c
                                 void* workspace, size_t ws_bytes, void* stream) {
     return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                            R, max_len, k, slots, scores, score_stride, workspace, ws_bytes, stream, true);
+}
+
+idx_status idx_score_topk_tagged(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                                 const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                                 int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                                 int64_t max_len, int k, uint32_t tag, int slots, int64_t* pairs, float* scores,
+                                 int64_t score_stride, void* workspace, size_t ws_bytes, void* stream) {
+    if (!pairs) return IDX_ERR_ARG;
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, nullptr, scores, score_stride, workspace, ws_bytes, stream, slots != 0,
+                           reinterpret_cast<long long*>(pairs), tag);
 }
 
 idx_status idx_quantize_query(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,

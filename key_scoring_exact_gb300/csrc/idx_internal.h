@@ -101,6 +101,10 @@ struct SelectArgs {
     const int32_t* slot_table = nullptr;
     const int32_t* slot_row_req = nullptr;
     int slot_max_pages = 0;
+    // When pairs is set, entry j of row r goes to pairs[r][j] as the int32
+    // words {entry, tag} (one 8-byte store) instead of indices[r][j].
+    long long* pairs = nullptr;
+    uint32_t tag = 0;
 };
 
 cudaError_t launch_select(const SelectArgs& a);

@@ -54,7 +54,8 @@
 //  * One block scan of the threads' packed (above T, at T) counts gives their
 //    offsets, and the positions are written in order: keys above T first,
 //    then ties, each in ascending position (or, for the slot variant, the
-//    cache slots those positions map to).
+//    cache slots those positions map to; for the tagged variant, each entry
+//    beside the launch's tag in one 8-byte store).
 #include "idx_internal.h"
 #include "ptx.cuh"
 
@@ -401,15 +402,28 @@ __device__ __forceinline__ void cand_round(const uint2* cand, int n, uint32_t pr
 // Words of a slice's radix keys in shared memory (a multiple of 4).
 __host__ __device__ constexpr int slice_words(int cap) { return (cap + 4 + 3) & ~3; }
 
-// List entries as positions, or as physical cache slots of the row's request.
+// List entries as positions, or as physical cache slots of the row's request;
+// with `pairs`, each entry is written as a tagged pair instead.
 struct SlotMap {
     const int32_t* table;    // [n_req][max_pages] page ids, or null for positions
     const int32_t* row_req;  // [R]
     int max_pages;
+    long long* pairs;        // [R][k] tagged pairs, or null: entries into `out`
+    uint32_t tag;
 };
 
 __device__ __forceinline__ int32_t list_entry(const int32_t* page_row, int64_t pos) {
     return page_row ? page_row[pos / kPage] * kPage + (int32_t)(pos % kPage) : (int32_t)pos;
+}
+
+// Entry j of the row's list: an int32, or the pair {entry, tag} (the int32
+// words in that order) in one 8-byte store, so that a reader that sees the
+// launch's tag in a pair sees that launch's entry beside it.
+__device__ __forceinline__ void put_entry(int32_t* dst, long long* pdst, uint32_t tag, int64_t j, int32_t e) {
+    if (pdst)
+        pdst[j] = (long long)(((unsigned long long)tag << 32) | (unsigned long long)(uint32_t)e);
+    else
+        dst[j] = e;
 }
 
 template <int CL>
@@ -470,10 +484,11 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         n = (int64_t)CL * slice_cap;
     }
     int32_t* dst = out + (int64_t)row * k;
+    long long* pdst = sm.pairs ? sm.pairs + (int64_t)row * k : nullptr;
     const int32_t* page_row = sm.table ? sm.table + (int64_t)sm.row_req[row] * sm.max_pages : nullptr;
     if (n <= k) {  // uniform over the cluster: no barrier is skipped by a subset
         if (c == 0)
-            for (int j = tid; j < k; j += kThreads) dst[j] = j < n ? list_entry(page_row, j) : -1;
+            for (int j = tid; j < k; j += kThreads) put_entry(dst, pdst, sm.tag, j, j < n ? list_entry(page_row, j) : -1);
         return;
     }
     const bool single = n <= slice_cap;
@@ -714,10 +729,10 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
                 const int i = 4 * j + q;
                 if (i >= cnt) break;
                 if (uu[q] > T) {
-                    if (pg < gt_total) dst[pg] = list_entry(page_row, start + i);
+                    if (pg < gt_total) put_entry(dst, pdst, sm.tag, pg, list_entry(page_row, start + i));
                     ++pg;
                 } else if (uu[q] == T) {
-                    if (pe < (uint32_t)k) dst[pe] = list_entry(page_row, start + i);
+                    if (pe < (uint32_t)k) put_entry(dst, pdst, sm.tag, pe, list_entry(page_row, start + i));
                     ++pe;
                 }
             }
@@ -786,7 +801,7 @@ cudaError_t launch_c(const SelectArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     const int64_t cap_len = a.len_cap < a.score_stride ? a.len_cap : a.score_stride;
-    const SlotMap sm{a.slot_table, a.slot_row_req, a.slot_max_pages};
+    const SlotMap sm{a.slot_table, a.slot_row_req, a.slot_max_pages, a.pairs, a.tag};
     return cudaLaunchKernelEx(&cfg, k_select<CL>, a.scores, cap_len, a.row_lens, a.score_stride, a.k, a.indices,
                               a.status, cap, sm);
 }

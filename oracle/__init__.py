@@ -70,6 +70,8 @@ def _load():
             lib.oracle_slots.argtypes = [p, i32, i32, p, i32, p, i32, p]
             lib.oracle_quantize_query.restype = None
             lib.oracle_quantize_query.argtypes = [p, p, i32, i32, i32, p, p]
+            lib.oracle_tagged.restype = None
+            lib.oracle_tagged.argtypes = [p, i64, ctypes.c_uint32, p]
             _lib = lib
     return _lib
 
@@ -137,6 +139,16 @@ def slots(idx, block_table, row_req, page: int = 64) -> np.ndarray:
     rr = _c(row_req, np.int32)
     out = np.empty(i.shape, np.int32)
     lib.oracle_slots(_ptr(i), i.shape[0], i.shape[1], _ptr(bt), bt.shape[1], _ptr(rr), int(page), _ptr(out))
+    return out
+
+
+def tagged(entries, tag: int) -> np.ndarray:
+    """List entries (positions or slots, -1 = padding) as tagged pairs: int64
+    words whose low 32 bits hold the entry and whose high 32 bits the tag."""
+    lib = _load()
+    e = _c(entries, np.int32)
+    out = np.empty(e.shape, np.int64)
+    lib.oracle_tagged(_ptr(e), e.size, int(tag) & 0xFFFFFFFF, _ptr(out))
     return out
 
 

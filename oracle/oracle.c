@@ -361,3 +361,15 @@ void oracle_slots(const int32_t *idx, int R, int k, const int32_t *block_table, 
                 p < 0 ? -1 : block_table[(size_t)row_req[r] * max_pages + p / page] * page + p % page;
         }
 }
+
+/* Tagged pairs ("sgl-amd-mono-upstream PR 11", section "3. The selected tokens
+ * are tagged pairs"): each list entry travels with the launch's tag, so a
+ * reader can tell this launch's entries from an earlier launch's without a
+ * separate flag.  The pair of entry e and tag t is the 64-bit word whose low
+ * 32 bits are e (as an unsigned 32-bit pattern) and whose high 32 bits are t.
+ * entries and out have n elements. */
+void oracle_tagged(const int32_t *entries, int64_t n, uint32_t tag, int64_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (int64_t)(((uint64_t)tag << 32) | (uint64_t)(uint32_t)entries[i]);
+}

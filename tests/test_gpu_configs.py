@@ -240,6 +240,29 @@ def test_slot_lists(cfg):
     assert np.array_equal(got.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("slots", [False, True])
+def test_tagged_pairs(slots):
+    """idx_score_topk_tagged: every pair is the oracle's tagged pair of the
+    oracle's list of the GPU's own scores (positions, or cache slots), padding
+    included; a second launch with another tag rewrites every pair."""
+    w = W.make_workload([W.chain(20000, 4), [1500], [0, 9000]], "recent", seed=77)
+    t = device_inputs(w)
+    stride = stride_for(w.max_len)
+    ws = binding.new_workspace(w.R, w.max_len, w.k)
+    for tag in (0xABCD1234, 0xFFFFFFFF):
+        scores = torch.zeros(w.R, stride, dtype=torch.float32, device="cuda")
+        pairs = torch.full((w.R, w.k), 0x5555555555555555, dtype=torch.int64, device="cuda")
+        binding.score_topk_tagged(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"],
+                                  t["seq_lens"], t["row_req"], w.max_len, w.k, tag, pairs, ws, scores=scores,
+                                  slots=slots)
+        assert binding.check_status(ws) == 0
+        s = scores.cpu().numpy()
+        lists = np.stack([oracle.topk(s[r, :n], w.k) for r, n in enumerate(w.seq_lens.tolist())])
+        if slots:
+            lists = oracle.slots(lists, w.block_table.numpy(), w.row_req.numpy())
+        assert np.array_equal(pairs.cpu().numpy(), oracle.tagged(lists, tag))
+
+
 def test_host_buffer_call_e4m3_query():
     """idx_score_topk_host with an E4M3 query (one byte per element)."""
     w = W.make_workload([W.chain(5000)], "random", seed=91, q_is_e4m3=True)

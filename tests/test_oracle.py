@@ -500,3 +500,22 @@ def test_slots_worked_example_and_closed_forms():
     ident = np.arange(64, dtype=np.int32)[None, :]
     pos = np.random.default_rng(3).integers(0, 64 * 64, (3, 50)).astype(np.int32)
     assert np.array_equal(oracle.slots(pos, ident, np.zeros(3, np.int32)), pos)
+
+
+def test_tagged_pairs_worked_example_and_layout():
+    """oracle_tagged ("sgl-amd-mono-upstream PR 11", section "3. The selected
+    tokens are tagged pairs"): worked values written out by hand, and the pair
+    read back as its two little-endian int32 words {entry, tag}."""
+    e = np.array([5, -1, 0x7FFFFFFF, 0, 2048], np.int32)
+    got = oracle.tagged(e, 7)
+    assert got.tolist() == [0x0000000700000005, 0x00000007FFFFFFFF, 0x000000077FFFFFFF,
+                            0x0000000700000000, 0x0000000700000800]
+    # the top tag bit: the int64 goes negative, the words stay {entry, tag}
+    top = oracle.tagged(np.array([3, -1], np.int32), 0xFFFFFFFF)
+    assert top.tolist() == [-(1 << 32) + 3, -1]
+    rng = np.random.default_rng(4)
+    ent = rng.integers(-1, 1 << 31, size=1000).astype(np.int32)
+    for tag in (0, 1, 123456789, 0xFFFFFFFF):
+        words = oracle.tagged(ent, tag).view(np.int32).reshape(-1, 2)   # little-endian host
+        assert np.array_equal(words[:, 0], ent)
+        assert np.all(words[:, 1].view(np.uint32) == np.uint32(tag))
