@@ -202,6 +202,37 @@ idx_status idx_score_topk_tagged(int qtype, const void *q, const float *head_w,
                                  void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_score_topk_newkeys -- idx_score_topk for a step whose rows bring new
+ * index keys: "sgl-amd-mono-upstream PR 18", section "Modifications / 2",
+ * keys this launch writes.  Row r's own key (its request's position
+ * seq_lens[r] - 1, the slot the row writes) is new_k[r] with scale
+ * new_scale[r]; the call stores it in the cache and every row of the request
+ * scores it, in whichever group of rows that row falls (an 8-row draft chain
+ * spans two groups, and the second group scores the first group's new keys).
+ * The store comes first, so the cache may hold anything at those slots before
+ * the call (stale or poisoned values).
+ *
+ *  k_cache, k_scale  as in idx_score, and written: slot seq_lens[r] - 1 of
+ *               request row_req[r] receives row r's key and scale (rows of one
+ *               request name distinct slots; rows with seq_lens[r] == 0 store
+ *               nothing; a slot whose block-table entry lies outside the pool
+ *               is skipped and reported as IDX_ERR_BOUNDS)
+ *  new_k        [R][IDX_DIM] E4M3 codes, 16-byte aligned
+ *  new_scale    [R] f32, >= 0
+ *
+ * The other arguments, the outputs and the errors are those of
+ * idx_score_topk.
+ */
+idx_status idx_score_topk_newkeys(int qtype, const void *q, const float *head_w,
+                                  uint8_t *k_cache, float *k_scale, int64_t pool_pages,
+                                  const int32_t *block_table, int max_pages,
+                                  const int32_t *seq_lens, const int32_t *row_req, int R,
+                                  const uint8_t *new_k, const float *new_scale,
+                                  int64_t max_len, int k, int32_t *indices,
+                                  float *scores, int64_t score_stride,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_quantize_query -- the FP8 (E4M3) query of a bf16 index query, one scale
  * per (row, head), as IDX_Q_BF16_FP8 scoring uses it.  The recipe is the
  * per-token FP8 quantisation of "[Perf] [MI355X] minimax_m31" (section

@@ -223,7 +223,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                           const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
                           size_t ws_bytes, void* stream, bool slots, long long* pairs = nullptr,
-                          uint32_t tag = 0) {
+                          uint32_t tag = 0, const uint8_t* new_k = nullptr, const float* new_scale = nullptr) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
@@ -248,6 +248,8 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ScoreArgs a{qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                 R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
+    a.new_k = new_k;
+    a.new_scale = new_scale;
     st = run_score(a);
     if (st != IDX_OK) return st;
     // Each row's selection covers the keys its scores were written for.
@@ -343,6 +345,18 @@ idx_status idx_score_topk_tagged(int qtype, const void* q, const float* head_w, 
     return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                            R, max_len, k, nullptr, scores, score_stride, workspace, ws_bytes, stream, slots != 0,
                            reinterpret_cast<long long*>(pairs), tag);
+}
+
+idx_status idx_score_topk_newkeys(int qtype, const void* q, const float* head_w, uint8_t* k_cache, float* k_scale,
+                                  int64_t pool_pages, const int32_t* block_table, int max_pages,
+                                  const int32_t* seq_lens, const int32_t* row_req, int R, const uint8_t* new_k,
+                                  const float* new_scale, int64_t max_len, int k, int32_t* indices, float* scores,
+                                  int64_t score_stride, void* workspace, size_t ws_bytes, void* stream) {
+    if (!new_k || !new_scale) return IDX_ERR_ARG;
+    if (!aligned(new_k, 16) || !aligned(new_scale, 4)) return IDX_ERR_ALIGN;
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false, nullptr, 0,
+                           new_k, new_scale);
 }
 
 idx_status idx_quantize_query(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,

@@ -71,6 +71,12 @@ struct ScoreArgs {
     WsLayout L;
     cudaStream_t stream;
     int num_sms;
+    // Keys this call stores: row r's key new_k[r] (128 E4M3 codes) and scale
+    // new_scale[r] go to its own cache slot, position seq_lens[r] - 1 of its
+    // request, before any row scores them (null: no store).  The cache
+    // pointers above are then written.
+    const uint8_t* new_k = nullptr;
+    const float* new_scale = nullptr;
 };
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);

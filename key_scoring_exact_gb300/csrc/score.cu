@@ -111,6 +111,10 @@ struct ScoreParams {
     int64_t score_stride;
     uint32_t* status;
     uint8_t* qop;            // the rows' prepared operands (k_qprep), or null: split in the kernel
+    const uint8_t* new_k;    // with qop: k_qprep stores each row's new key and scale in its slot
+    const float* new_scale;
+    uint8_t* k_cache_w;      // the cache, written by that store
+    float* k_scale_w;
     uint64_t wait_ns;        // wall-time limit of every role's waits (kWaitTimeoutNs in normal use)
     int drop_query_handoff;  // test only: the epilogue never signals the query operand
 };
@@ -367,6 +371,26 @@ __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
     const int lane = threadIdx.x & 31;
     const int warp_g = blockIdx.x * (kQprepThreads / 32) + (threadIdx.x >> 5);
     const int pairs = p.R * kHeads;
+    if (p.new_k && warp_g < p.R) {
+        // The keys this call writes ("sgl-amd-mono-upstream PR 18", section
+        // "Modifications / 2", keys this launch writes): row r's key goes to its
+        // own slot, position seq_lens[r] - 1 of its request, so that every row
+        // of the request -- in any row group -- scores it.  The scoring's
+        // producer waits for this grid before its first page load.
+        const int r = warp_g;
+        const int len = __ldcg(p.seq_lens + r), req = __ldcg(p.row_req + r);
+        if (len >= 1 && (int64_t)len <= p.len_cap && req >= 0) {
+            const int pos = len - 1;
+            const int v = __ldcg(p.block_table + (int64_t)req * p.max_pages + pos / kPage);
+            if (v >= 0 && (int64_t)v < p.pool_pages) {
+                reinterpret_cast<uint32_t*>(p.k_cache_w + (int64_t)v * kPageKeyBytes + (pos % kPage) * kDim)[lane] =
+                    reinterpret_cast<const uint32_t*>(p.new_k + (int64_t)r * kDim)[lane];
+                if (lane == 0) p.k_scale_w[(int64_t)v * kPage + pos % kPage] = p.new_scale[r];
+            } else if (lane == 0) {
+                record_status(p.status, kStatusBounds);
+            }
+        }
+    }
     uint8_t* hi = p.qop;
     uint8_t* lo = p.qop + (int64_t)p.R * kQRowBytes;
     float* wq = reinterpret_cast<float*>(p.qop + 2 * (int64_t)p.R * kQRowBytes);
@@ -505,7 +529,10 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
         // ------------------------------------------------------ TMA producer
         // The whole warp fetches block-table entries, one page per lane and
         // up to 16 tiles at a time, so the page ids of a batch arrive in one
-        // round trip; lane 0 waits on the ring and issues the copies.
+        // round trip; lane 0 waits on the ring and issues the copies.  When
+        // k_qprep stores this call's keys, the pages are loaded only after it
+        // has completed.
+        if (p.new_k) pdl_wait();
         int g = find_group(pl, n_groups, it0), issued = 0;
         bool stop = false;
         int it = it0;
@@ -795,6 +822,11 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.score_stride = a.score_stride;
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
     p.qop = a.L.qop ? reinterpret_cast<uint8_t*>(a.ws + a.L.qop) : nullptr;
+    if (a.new_k && !p.qop) return cudaErrorInvalidValue;  // the store is k_qprep's
+    p.new_k = a.new_k;
+    p.new_scale = a.new_scale;
+    p.k_cache_w = const_cast<uint8_t*>(a.k_cache);
+    p.k_scale_w = const_cast<float*>(a.k_scale);
     const WaitTestHook hook = wait_test_hook();
     p.wait_ns = hook.wait_ns ? hook.wait_ns : kWaitTimeoutNs;
     p.drop_query_handoff = hook.drop_query_handoff;

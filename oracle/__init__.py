@@ -72,6 +72,8 @@ def _load():
             lib.oracle_quantize_query.argtypes = [p, p, i32, i32, i32, p, p]
             lib.oracle_tagged.restype = None
             lib.oracle_tagged.argtypes = [p, i64, ctypes.c_uint32, p]
+            lib.oracle_store_keys.restype = i32
+            lib.oracle_store_keys.argtypes = [p, p, i64, p, i32, p, p, i32, p, p, i32, i32]
             _lib = lib
     return _lib
 
@@ -140,6 +142,25 @@ def slots(idx, block_table, row_req, page: int = 64) -> np.ndarray:
     out = np.empty(i.shape, np.int32)
     lib.oracle_slots(_ptr(i), i.shape[0], i.shape[1], _ptr(bt), bt.shape[1], _ptr(rr), int(page), _ptr(out))
     return out
+
+
+def store_keys(k_cache, k_scale, block_table, seq_lens, row_req, new_k, new_scale, page: int = 64):
+    """The cache after the step's stores: row r's key new_k[r] and scale
+    new_scale[r] in its slot, position seq_lens[r] - 1 of its request.
+    Returns new (k_cache, k_scale) arrays; the inputs are not changed."""
+    lib = _load()
+    kc = np.array(k_cache, np.uint8, copy=True, order="C")
+    ks = np.array(k_scale, np.float32, copy=True, order="C")
+    bt = _c(block_table, np.int32)
+    ln = _c(seq_lens, np.int32)
+    rr = _c(row_req, np.int32)
+    nk = _c(new_k, np.uint8)
+    ns = _c(new_scale, np.float32)
+    st = lib.oracle_store_keys(_ptr(kc), _ptr(ks), kc.shape[0], _ptr(bt), bt.shape[1], _ptr(ln), _ptr(rr),
+                               ln.shape[0], _ptr(nk), _ptr(ns), int(page), kc.shape[2])
+    if st != OK:
+        raise ValueError("oracle_store_keys: a slot's page is outside the pool")
+    return kc, ks
 
 
 def tagged(entries, tag: int) -> np.ndarray:

@@ -519,3 +519,61 @@ def test_tagged_pairs_worked_example_and_layout():
         words = oracle.tagged(ent, tag).view(np.int32).reshape(-1, 2)   # little-endian host
         assert np.array_equal(words[:, 0], ent)
         assert np.all(words[:, 1].view(np.uint32) == np.uint32(tag))
+
+
+def test_store_keys_worked_example():
+    """oracle_store_keys ("sgl-amd-mono-upstream PR 18", section "Modifications
+    / 2", keys this launch writes): each row's key lands in the slot of its
+    request's position seq_lens[r] - 1, found through the block table, and
+    nothing else changes.  The expected cache is written by hand."""
+    P, D = 64, 128
+    rng = np.random.default_rng(8)
+    kc = rng.integers(0, 256, size=(3, P, D), dtype=np.uint8)
+    ks = rng.random((3, P), dtype=np.float32)
+    bt = np.array([[2, 0], [1, -1]], np.int32)       # request 0: page 2 then page 0; request 1: page 1
+    lens = np.array([70, 65, 0, 10], np.int32)        # rows 0..2 of request 0, row 3 of request 1
+    rreq = np.array([0, 0, 0, 1], np.int32)
+    nk = rng.integers(0, 256, size=(4, D), dtype=np.uint8)
+    ns = np.array([0.5, 1.5, 9.0, 2.5], np.float32)
+    got_k, got_s = oracle.store_keys(kc, ks, bt, lens, rreq, nk, ns)
+    want_k, want_s = kc.copy(), ks.copy()
+    want_k[0, 5] = nk[0]      # row 0: position 69 = page index 1 -> page 0, slot 5
+    want_s[0, 5] = 0.5
+    want_k[0, 0] = nk[1]      # row 1: position 64 -> page 0, slot 0
+    want_s[0, 0] = 1.5
+    want_k[1, 9] = nk[3]      # row 3: position 9 of request 1 -> page 1, slot 9 (row 2 has no key)
+    want_s[1, 9] = 2.5
+    assert np.array_equal(got_k, want_k) and np.array_equal(got_s, want_s)
+    assert np.array_equal(kc, oracle.store_keys(kc, ks, bt, lens * 0, rreq, nk, ns)[0])  # no keys: no change
+
+
+def test_stored_keys_are_what_the_rows_score():
+    """After the store, the score of each new key is the one-hot closed form
+    of that key (head 0 only, w = 1): scale * e4m3(code) * q where positive;
+    with the slot poisoned and no store, the same score is not finite."""
+    P, D, H = 64, 128, 64
+    R = 3
+    kc = np.zeros((2, P, D), np.uint8)
+    ks = np.ones((2, P), np.float32)
+    bt = np.array([[1, 0]], np.int32)
+    lens = np.array([70, 71, 72], np.int32)
+    rreq = np.zeros(R, np.int32)
+    kc[0, 5:8] = 0x7F                                  # the rows' slots poisoned (NaN codes, huge scales)
+    ks[0, 5:8] = 1e30
+    nk = np.zeros((R, D), np.uint8)
+    nk[:, 3] = [0x38, 0x40, 0x44]                      # 1.0, 2.0, 3.0 in E4M3, at dim 3
+    ns = np.array([0.5, 1.5, 2.0], np.float32)
+    q = np.zeros((R, H, D), np.float32)
+    q[:, 0, 3] = 1.0
+    qb = (torch.from_numpy(q).to(torch.bfloat16).view(torch.uint16).numpy())
+    w = np.zeros((R, H), np.float32)
+    w[:, 0] = 1.0
+    kc2, ks2 = oracle.store_keys(kc, ks, bt, lens, rreq, nk, ns)
+    s = oracle.scores(oracle.Problem(qb, False, w, kc2, ks2, bt, lens, rreq))
+    for r in range(R):
+        for j, (code_val, sc) in enumerate([(1.0, 0.5), (2.0, 1.5), (3.0, 2.0)]):
+            pos = 69 + j
+            if pos < lens[r]:
+                assert s[r, pos] == code_val * sc, (r, pos, s[r, pos])
+    poisoned = oracle.scores(oracle.Problem(qb, False, w, kc, ks, bt, lens, rreq))
+    assert not np.isfinite(poisoned[2, 69:72]).any()
