@@ -62,6 +62,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-8k", action="store_true")
     ap.add_argument("--no-fp8q", action="store_true", help="skip the FP8-query measurement")
+    ap.add_argument("--no-newkeys", action="store_true", help="skip the new-key-store measurement")
     ap.add_argument("--no-batch", action="store_true", help="skip the 64-row measurement")
     ap.add_argument("--no-warm", action="store_true", help="skip the L2-resident measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
@@ -237,8 +238,16 @@ class Step:
 
     quantize_q = False  # score the on-device FP8 quantisation of the bf16 query
 
+    new_keys = None  # (new_k [R, 128] E4M3 codes, new_scale [R]): each step stores its rows' keys first
+
     def fused(self, c, stream=None):
         b = self.binding
+        if self.new_keys is not None:
+            b.score_topk_newkeys(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
+                                 self.seq_lens, self.row_req, self.new_keys[0], self.new_keys[1], self.max_len,
+                                 self.k, self.idx, self.ws, scores=self.scores, stream=stream,
+                                 quantize_q=self.quantize_q)
+            return
         b.score_topk(self.q, self.head_w, self.k_cache, self.k_scale, self.tables[c % self.copies],
                      self.seq_lens, self.row_req, self.max_len, self.k, self.idx, self.ws,
                      scores=self.scores, stream=stream, quantize_q=self.quantize_q)
@@ -635,6 +644,19 @@ def main():
         line["also_fp8_query"] = {"workload": w.recipe + "; query quantised to E4M3 on the device per (row, head)",
                                   "us": secq * 1e6, "scoring_us": tq_score * 1e6,
                                   "keys_per_s": w.row_keys() / secq}
+    if not args.no_newkeys:
+        # the same workload as a decode step that brings its rows' own keys:
+        # every step stores each row's key in its slot, then scores and selects
+        g = torch.Generator().manual_seed(7)
+        st.new_keys = (torch.randn(w.R, 128, generator=g).to(torch.float8_e4m3fn).view(torch.uint8).to(dev),
+                       (torch.rand(w.R, generator=g) * 1.5 + 0.5).to(dev))
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                st.fused(i, stream)
+            secn, _ = time_graph_steps(st, min(args.steps, 4096), stream, None)
+        st.new_keys = None
+        line["also_new_keys"] = {"workload": w.recipe + "; each step first stores its rows' new keys "
+                                 "(idx_score_topk_newkeys)", "us": secn * 1e6, "keys_per_s": w.row_keys() / secn}
     if not args.no_e2e:
         e2e_sec, h2d, d2h = e2e_time(st, min(args.steps, 200), stream)
         line["e2e"] = {"value": e2e_sec * 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
