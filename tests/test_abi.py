@@ -126,3 +126,26 @@ def test_host_entry_sizes_and_argument_errors(lib):
     long_rows = list(args)
     long_rows[8], long_rows[12] = 10000, 600000                  # rows past the selection's 524,288 keys
     assert lib.idx_score_topk_host(*long_rows) == -1
+
+
+def test_tagged_and_newkeys_argument_errors_need_no_gpu(lib):
+    """idx_score_topk_tagged and idx_score_topk_newkeys refuse a null or
+    misaligned output or key array before anything is launched."""
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    common = [i32, p, p, p, p, i64, p, i32, p, p, i32]
+    lib.idx_score_topk_tagged.restype = i32
+    lib.idx_score_topk_tagged.argtypes = common + [i64, i32, ctypes.c_uint32, i32, p, p, i64, p, sz, p]
+    lib.idx_score_topk_newkeys.restype = i32
+    lib.idx_score_topk_newkeys.argtypes = common + [p, p, i64, i32, p, p, i64, p, sz, p]
+    fake = ctypes.c_void_p(1 << 20)
+    base = [0, fake, fake, fake, fake, 8, fake, 4, fake, fake, 2]
+    tag = lambda pairs: lib.idx_score_topk_tagged(*base, 256, 16, 7, 0, pairs, None, 0, fake, 1 << 30, None)
+    assert tag(None) == -1                               # no output
+    assert tag(ctypes.c_void_p((1 << 20) + 4)) == -2     # pairs not 8-byte aligned
+    newk = lambda nk, ns: lib.idx_score_topk_newkeys(*base, nk, ns, 256, 16, fake, None, 0, fake, 1 << 30, None)
+    assert newk(None, fake) == -1                        # no new keys
+    assert newk(fake, None) == -1                        # no new scales
+    assert newk(ctypes.c_void_p((1 << 20) + 8), fake) == -2  # keys not 16-byte aligned
+    bad_type = list(base)
+    bad_type[0] = 9
+    assert lib.idx_score_topk_newkeys(*bad_type, fake, fake, 256, 16, fake, None, 0, fake, 1 << 30, None) == -1

@@ -21,12 +21,14 @@ pytestmark = pytest.mark.gpu
 E4M3_NAN = 0x7F
 
 
-@pytest.mark.parametrize("layout", [
-    [W.chain(20000, 8), [3000]],      # an 8-row draft chain: two row groups, each scoring the other's keys
-    [W.chain(9000, 4), [700], W.chain(5000, 3)],
+@pytest.mark.parametrize("layout,query", [
+    ([W.chain(20000, 8), [3000]], "bf16"),   # an 8-row draft chain: two row groups, each scoring the other's keys
+    ([W.chain(9000, 4), [700], W.chain(5000, 3)], "bf16"),
+    ([W.chain(6000, 6)], "e4m3"),
+    ([W.chain(6000, 6), [2500]], "bf16_fp8"),
 ])
-def test_new_keys_stored_and_scored_by_every_row(layout):
-    w = W.make_workload(layout, "random", seed=sum(map(sum, layout)) % 97)
+def test_new_keys_stored_and_scored_by_every_row(layout, query):
+    w = W.make_workload(layout, "random", seed=sum(map(sum, layout)) % 97, q_is_e4m3=query == "e4m3")
     R = w.R
     g = torch.Generator().manual_seed(123)
     new_k = torch.randn(R, 128, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
@@ -47,15 +49,20 @@ def test_new_keys_stored_and_scored_by_every_row(layout):
     ws = binding.new_workspace(R, w.max_len, w.k)
     binding.score_topk_newkeys(dev["q"], dev["head_w"], kc_d, ks_d, dev["block_table"], dev["seq_lens"],
                                dev["row_req"], new_k.cuda(), new_scale.cuda(), w.max_len, w.k, idx, ws,
-                               scores=scores)
+                               scores=scores, quantize_q=query == "bf16_fp8")
     assert binding.check_status(ws) == 0
     assert np.array_equal(kc_d.cpu().numpy(), want_k)
     # bit patterns: the pool's unused slots hold NaN scales
     assert np.array_equal(ks_d.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
 
     s = scores.cpu().numpy()
-    ref = oracle.scores(oracle.Problem(w.q_bits().numpy(), w.q_is_e4m3, w.head_w.numpy(), want_k, want_s, bt,
-                                       w.seq_lens.numpy(), w.row_req.numpy()))
+    if query == "bf16_fp8":   # the scores of the query as the device quantises it (idx_quantize_query)
+        q8, wq = oracle.quantize_query(w.q_bits().numpy(), w.head_w.numpy())
+        pb = oracle.Problem(q8, True, wq, want_k, want_s, bt, w.seq_lens.numpy(), w.row_req.numpy())
+    else:
+        pb = oracle.Problem(w.q_bits().numpy(), w.q_is_e4m3, w.head_w.numpy(), want_k, want_s, bt,
+                            w.seq_lens.numpy(), w.row_req.numpy())
+    ref = oracle.scores(pb)
     errs = checks.score_errors(s, ref, w.seq_lens.tolist())
     assert max(errs) <= checks.SCORE_TOL, errs
     got = idx.cpu().numpy()
