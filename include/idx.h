@@ -233,6 +233,37 @@ idx_status idx_score_topk_newkeys(int qtype, const void *q, const float *head_w,
                                   void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_score_topk_prefix_order -- idx_score_topk whose lists are in the
+ * pages' order ("sgl-amd-mono-upstream PR 18", section "Modifications / 3",
+ * Order, and section "Modifications / 0", the list check): the pages' radix
+ * stops at the first of the threshold's 12- and 24-bit prefixes whose keys
+ * fit the candidate room, else at all 32 bits.  With T the k-th largest
+ * score's order-preserving 32-bit image (as the selection uses it) and P the
+ * first of T's 12- and 24-bit prefixes shared by at most `room` of the row's
+ * keys (else all 32 bits), row r's list is
+ *     the keys whose image's prefix is above P, in ascending position;
+ *     then the keys with prefix P above T, in ascending position;
+ *     then the keys equal to T, in ascending position, until k entries.
+ * It holds the same keys as idx_score_topk's list; at 32 bits (room 0, or
+ * T's prefixes shared too widely) it is that list.  The pages do not size
+ * the room; the caller gives it.  Rows with at most k keys are as in
+ * idx_score_topk.
+ *
+ *  room      the candidate room, >= 0 (else IDX_ERR_ARG)
+ *  indices   [R][k] int32 out, logical positions
+ *
+ * The other arguments and the errors are those of idx_score_topk.  One more
+ * launch after the selection reads each row's scores once more.
+ */
+idx_status idx_score_topk_prefix_order(int qtype, const void *q, const float *head_w,
+                                       const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                                       const int32_t *block_table, int max_pages,
+                                       const int32_t *seq_lens, const int32_t *row_req, int R,
+                                       int64_t max_len, int k, int64_t room, int32_t *indices,
+                                       float *scores, int64_t score_stride,
+                                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_quantize_query -- the FP8 (E4M3) query of a bf16 index query, one scale
  * per (row, head), as IDX_Q_BF16_FP8 scoring uses it.  The recipe is the
  * per-token FP8 quantisation of "[Perf] [MI355X] minimax_m31" (section

@@ -23,7 +23,7 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
            "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots",
-           "idx_score_topk_tagged", "idx_score_topk_newkeys")
+           "idx_score_topk_tagged", "idx_score_topk_newkeys", "idx_score_topk_prefix_order")
 DIAG_EXPORTS = ("idx_probe_fp8_mma", "idx_test_set_wait_limit")   # include/idx_diag.h
 
 _lib = None
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_score_topk.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
     lib.idx_score_topk_slots.restype = i32
     lib.idx_score_topk_slots.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
+    lib.idx_score_topk_prefix_order.restype = i32
+    lib.idx_score_topk_prefix_order.argtypes = score_common + [i64, i32, i64, p, p, i64, p, sz, p]
     lib.idx_score_topk_newkeys.restype = i32
     lib.idx_score_topk_newkeys.argtypes = score_common + [p, p, i64, i32, p, p, i64, p, sz, p]
     lib.idx_score_topk_tagged.restype = i32
@@ -238,6 +240,22 @@ def score_topk_tagged(q, head_w, k_cache, k_scale, block_table, seq_lens, row_re
                                       _dev(pairs, "pairs", torch.int64), sp, stride,
                                       _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "idx_score_topk_tagged")
+
+
+def score_topk_prefix_order(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, room, indices,
+                            workspace, scores=None, stream=None, quantize_q=False):
+    """idx_score_topk_prefix_order: as score_topk, each list in the pages'
+    prefix order for candidate room `room`."""
+    args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
+    if indices.shape != (q.shape[0], k):
+        raise ValueError("indices must be [R, k]")
+    sp = _dev(scores, "scores", torch.float32) if scores is not None else None
+    stride = int(scores.shape[1]) if scores is not None else 0
+    st = load().idx_score_topk_prefix_order(*args, int(max_len), int(k), int(room),
+                                            _dev(indices, "indices", torch.int32), sp, stride,
+                                            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                                            _stream(stream))
+    _check(st, "idx_score_topk_prefix_order")
 
 
 def score_topk_newkeys(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, new_k, new_scale, max_len, k,

@@ -223,7 +223,8 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                           const int32_t* seq_lens, const int32_t* row_req, int R, int64_t max_len, int k,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
                           size_t ws_bytes, void* stream, bool slots, long long* pairs = nullptr,
-                          uint32_t tag = 0, const uint8_t* new_k = nullptr, const float* new_scale = nullptr) {
+                          uint32_t tag = 0, const uint8_t* new_k = nullptr, const float* new_scale = nullptr,
+                          int64_t prefix_room = -1) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
@@ -262,7 +263,9 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
     }
     sel.pairs = pairs;
     sel.tag = tag;
-    return to_status(launch_select(sel));
+    const cudaError_t e = launch_select(sel);
+    if (e != cudaSuccess || prefix_room < 0) return to_status(e);
+    return to_status(launch_prefix_order(sel, prefix_room));
 }
 
 extern "C" {
@@ -357,6 +360,17 @@ idx_status idx_score_topk_newkeys(int qtype, const void* q, const float* head_w,
     return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                            R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false, nullptr, 0,
                            new_k, new_scale);
+}
+
+idx_status idx_score_topk_prefix_order(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                                       const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                                       int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                                       int64_t max_len, int k, int64_t room, int32_t* indices, float* scores,
+                                       int64_t score_stride, void* workspace, size_t ws_bytes, void* stream) {
+    if (room < 0) return IDX_ERR_ARG;
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false, nullptr, 0,
+                           nullptr, nullptr, room);
 }
 
 idx_status idx_quantize_query(const void* q, const float* head_w, int R, uint8_t* q8, float* w_out,

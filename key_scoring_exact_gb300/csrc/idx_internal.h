@@ -114,6 +114,9 @@ struct SelectArgs {
 };
 
 cudaError_t launch_select(const SelectArgs& a);
+// After launch_select on the same stream: each row's list rearranged into the
+// pages' prefix order for candidate room `room` (position lists only).
+cudaError_t launch_prefix_order(const SelectArgs& a, int64_t room);
 
 // Device copies of host buffers the GPU can address (page-locked, mapped):
 // every source and destination 16-byte aligned, every size a multiple of 4.

@@ -740,6 +740,143 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
     }
 }
 
+// ---- the pages' list order --------------------------------------------------
+//
+// "sgl-amd-mono-upstream PR 18", section "Modifications / 3", Order: the
+// pages' radix stops at the first of the threshold's 12- and 24-bit prefixes
+// whose keys fit the candidate room, else at 32 bits, and its list is the keys
+// whose prefix is above the threshold's, in position order, then the prefix's
+// keys above the threshold, then the ties.  The pages do not size the room;
+// the caller gives it.  Given a row's list in this library's order (keys above
+// T, then ties, each in ascending position) this launch finds T (the smallest
+// image on the list), counts the row's keys sharing T's 12- and 24-bit
+// prefixes, and partitions the list stably into the three parts.
+constexpr int kOrderThreads = 512;
+constexpr int kOrderWarps = kOrderThreads / 32;
+
+// Exclusive sums over the block in thread order of three counts at once.
+__device__ __forceinline__ void order_scan3(uint32_t (&v)[3], uint32_t (&tot)[3], uint32_t* ws) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t inc[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        inc[c] = v[c];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, inc[c], o);
+            if (lane >= o) inc[c] += x;
+        }
+        if (lane == 31) ws[c * kOrderWarps + warp] = inc[c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const uint32_t wv = lane < kOrderWarps ? ws[c * kOrderWarps + lane] : 0u;
+        uint32_t wi = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, wi, o);
+            if (lane >= o) wi += x;
+        }
+        const uint32_t before = __shfl_sync(kFull, wi - wv, warp);
+        tot[c] = __shfl_sync(kFull, wi, 31);
+        v[c] = before + inc[c] - v[c];
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kOrderThreads)
+k_prefix_order(const float* __restrict__ scores, int64_t len_cap, const int32_t* __restrict__ row_lens, int64_t stride,
+               int k, int64_t room, int32_t* __restrict__ out) {
+    __shared__ int32_t lst[IDX_MAX_K];
+    __shared__ uint32_t img[IDX_MAX_K];
+    __shared__ uint32_t ws[3 * kOrderWarps];
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();
+    pdl_wait();  // the selection's list is complete
+    int64_t n = row_lens[row];
+    n = n < 0 ? 0 : (n > len_cap ? len_cap : n);
+    if (n <= k) return;  // every key, then -1: the same in every order
+    int32_t* dst = out + (int64_t)row * k;
+    const float* srow = scores + (int64_t)row * stride;
+    // the list, its keys' images, and T: the smallest image on it
+    uint32_t tmin = 0xFFFFFFFFu;
+    for (int j = tid; j < k; j += kOrderThreads) {
+        const int32_t p = dst[j];
+        const uint32_t u = (p >= 0 && p < n) ? radix_key(srow[p]) : 0xFFFFFFFFu;
+        lst[j] = p;
+        img[j] = u;
+        tmin = min(tmin, u);
+    }
+    tmin = __reduce_min_sync(kFull, tmin);
+    if (lane == 0) ws[warp] = tmin;
+    __syncthreads();
+    const uint32_t T = __reduce_min_sync(kFull, lane < kOrderWarps ? ws[lane] : 0xFFFFFFFFu);
+    __syncthreads();
+    // the row's keys sharing T's 12- and 24-bit prefixes
+    uint32_t c12 = 0, c24 = 0;
+    const int n4 = (int)((n + 3) >> 2);
+    const float4* src4 = reinterpret_cast<const float4*>(srow);
+    for (int i = tid; i < n4; i += kOrderThreads) {
+        const float4 v = __ldcg(src4 + i);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (4 * (int64_t)i + q < n) {
+                const uint32_t u = radix_key(f[q]);
+                c12 += (uint32_t)((u >> 20) == (T >> 20));
+                c24 += (uint32_t)((u >> 8) == (T >> 8));
+            }
+        }
+    }
+    c12 = __reduce_add_sync(kFull, c12);
+    c24 = __reduce_add_sync(kFull, c24);
+    if (lane == 0) {
+        ws[warp] = c12;
+        ws[kOrderWarps + warp] = c24;
+    }
+    __syncthreads();
+    const uint32_t n12 = __reduce_add_sync(kFull, lane < kOrderWarps ? ws[lane] : 0u);
+    const uint32_t n24 = __reduce_add_sync(kFull, lane < kOrderWarps ? ws[kOrderWarps + lane] : 0u);
+    __syncthreads();
+    const int sh = (int64_t)n12 <= room ? 20 : ((int64_t)n24 <= room ? 8 : 0);
+    const uint32_t tp = T >> sh;
+    // stable partition of the list: prefix above (0), prefix equal and above T (1), ties (2)
+    const int per = (k + kOrderThreads - 1) / kOrderThreads;
+    const int j0 = min(k, tid * per), j1 = min(k, j0 + per);
+    uint32_t cnt[3] = {0u, 0u, 0u};
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t u = img[j];
+        cnt[(u >> sh) > tp ? 0 : (u > T ? 1 : 2)] += 1u;
+    }
+    uint32_t tot[3];
+    order_scan3(cnt, tot, ws);
+    uint32_t at[3] = {cnt[0], tot[0] + cnt[1], tot[0] + tot[1] + cnt[2]};
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t u = img[j];
+        const int c = (u >> sh) > tp ? 0 : (u > T ? 1 : 2);
+        dst[at[c]++] = lst[j];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefix_order(const SelectArgs& a, int64_t room) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.R, 1, 1);
+    cfg.blockDim = dim3(kOrderThreads, 1, 1);
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t cap_len = a.len_cap < a.score_stride ? a.len_cap : a.score_stride;
+    return cudaLaunchKernelEx(&cfg, k_prefix_order, a.scores, cap_len, a.row_lens, a.score_stride, a.k, room, a.indices);
+}
+
+namespace {
+
 int slice_cap_for(int cl, int64_t max_len) {
     int64_t ns = (max_len + kSliceTarget - 1) / kSliceTarget;
     if (ns > cl) ns = cl;

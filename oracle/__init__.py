@@ -72,6 +72,8 @@ def _load():
             lib.oracle_quantize_query.argtypes = [p, p, i32, i32, i32, p, p]
             lib.oracle_tagged.restype = None
             lib.oracle_tagged.argtypes = [p, i64, ctypes.c_uint32, p]
+            lib.oracle_prefix_order.restype = i32
+            lib.oracle_prefix_order.argtypes = [p, i64, i32, i64, p]
             lib.oracle_store_keys.restype = i32
             lib.oracle_store_keys.argtypes = [p, p, i64, p, i32, p, p, i32, p, p, i32, i32]
             _lib = lib
@@ -237,6 +239,19 @@ def topk(row_scores, k: int) -> np.ndarray:
     st = lib.oracle_topk(_ptr(s), s.shape[0], int(k), _ptr(out))
     if st != OK:
         raise ValueError("oracle_topk failed with status %d" % st)
+    return out
+
+
+def prefix_order(row_scores, k: int, room: int) -> np.ndarray:
+    """One row's list in the pages' prefix order: the radix stops at the
+    threshold's 12- or 24-bit prefix once the row's keys sharing it number at
+    most `room`, else at 32 bits (oracle_topk's order)."""
+    lib = _load()
+    s = _c(row_scores, np.float32)
+    out = np.empty(k, np.int32)
+    st = lib.oracle_prefix_order(_ptr(s), s.shape[0], int(k), int(room), _ptr(out))
+    if st != OK:
+        raise ValueError("oracle_prefix_order failed with status %d" % st)
     return out
 
 

@@ -400,3 +400,76 @@ int oracle_store_keys(uint8_t *k_cache, float *k_scale, int64_t pool_pages, cons
     }
     return st;
 }
+
+/* ------------------------------------------- the pages' prefix list order */
+
+/* The order-preserving 32-bit image of a score that the pages' radix select
+ * works on ("sgl-amd-mono-upstream PR 18", section "Modifications / 3", keys
+ * held "as radix keys"): the IEEE-754 bits with the sign bit set for a
+ * non-negative value and every bit flipped for a negative one, so images
+ * compare as the values do; -0 counts as +0 and a NaN as the lowest image. */
+static uint32_t radix_image(float x)
+{
+    uint32_t b;
+    if (isnan(x))
+        return 0u;
+    memcpy(&b, &x, sizeof b);
+    if (b == 0x80000000u)
+        b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+/* The list of one row in the pages' order ("sgl-amd-mono-upstream PR 18",
+ * section "Modifications / 0", the list check, and "Modifications / 3",
+ * Order): the radix stops at the first of the threshold's 12- and 24-bit
+ * prefixes whose keys (the row's keys whose image shares that prefix with the
+ * k-th largest, T) number at most `room`, else it runs to all 32 bits.  With
+ * the stopping prefix P the list is
+ *   the keys whose prefix is above P, in position order;
+ *   then the keys with prefix P that rank above T, in position order;
+ *   then the keys tied with T, in position order, until k entries.
+ * At 32 bits the middle part is empty and the list is oracle_topk's; the set
+ * is oracle_topk's at every stop.  Rows with n <= k: as oracle_topk. */
+int oracle_prefix_order(const float *scores, int64_t n, int k, int64_t room, int32_t *out)
+{
+    scored_pos *v;
+    uint32_t t, p12, p24, tp;
+    int64_t j, c12 = 0, c24 = 0;
+    int filled = 0, sh;
+
+    if (k <= 0 || n < 0 || (n > 0 && !scores) || !out || room < 0)
+        return OR_ERR_ARG;
+    if (n <= k)
+        return oracle_topk(scores, n, k, out);
+    v = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+    if (!v)
+        return OR_ERR_ARG;
+    for (j = 0; j < n; ++j) {
+        v[j].s = scores[j];
+        v[j].pos = (int32_t)j;
+    }
+    qsort(v, (size_t)n, sizeof(scored_pos), cmp_desc_then_pos);
+    t = radix_image(v[k - 1].s); /* the k-th largest, counting repeats */
+    free(v);
+    p12 = t >> 20;
+    p24 = t >> 8;
+    for (j = 0; j < n; ++j) {
+        const uint32_t u = radix_image(scores[j]);
+        c12 += (u >> 20) == p12;
+        c24 += (u >> 8) == p24;
+    }
+    sh = c12 <= room ? 20 : (c24 <= room ? 8 : 0);
+    tp = t >> sh;
+    for (j = 0; j < n && filled < k; ++j)
+        if ((radix_image(scores[j]) >> sh) > tp)
+            out[filled++] = (int32_t)j;
+    for (j = 0; j < n && filled < k; ++j) {
+        const uint32_t u = radix_image(scores[j]);
+        if ((u >> sh) == tp && u > t)
+            out[filled++] = (int32_t)j;
+    }
+    for (j = 0; j < n && filled < k; ++j)
+        if (radix_image(scores[j]) == t)
+            out[filled++] = (int32_t)j;
+    return OR_OK;
+}

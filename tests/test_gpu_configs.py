@@ -263,6 +263,32 @@ def test_tagged_pairs(slots):
         assert np.array_equal(pairs.cpu().numpy(), oracle.tagged(lists, tag))
 
 
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+@pytest.mark.parametrize("room", [0, 64, 1024, 1 << 20])
+def test_prefix_order_lists(cfg, room):
+    """idx_score_topk_prefix_order: every list equals the oracle's list in the
+    pages' prefix order (of the GPU's own scores) for the given candidate room;
+    room 0 gives idx_score_topk's lists."""
+    w = W.make_config(cfg)
+    t = device_inputs(w)
+    scores = torch.zeros(w.R, stride_for(w.max_len), dtype=torch.float32, device="cuda")
+    idx = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+    ws = binding.new_workspace(w.R, w.max_len, w.k)
+    binding.score_topk_prefix_order(t["q"], t["head_w"], t["k_cache"], t["k_scale"], t["block_table"],
+                                    t["seq_lens"], t["row_req"], w.max_len, w.k, room, idx, ws, scores=scores)
+    assert binding.check_status(ws) == 0
+    s = scores.cpu().numpy()
+    got = idx.cpu().numpy()
+    differ = 0
+    for r, n in enumerate(w.seq_lens.tolist()):
+        assert np.array_equal(got[r], oracle.prefix_order(s[r, :n], w.k, room)), "row %d" % r
+        differ += int(not np.array_equal(got[r], oracle.topk(s[r, :n], w.k)))
+    if room == 0:
+        assert differ == 0
+    if room == 1 << 20 and cfg in (1, 4):
+        assert differ > 0, "the prefix order should differ from the specification's order here"
+
+
 def test_host_buffer_call_e4m3_query():
     """idx_score_topk_host with an E4M3 query (one byte per element)."""
     w = W.make_workload([W.chain(5000)], "random", seed=91, q_is_e4m3=True)

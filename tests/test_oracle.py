@@ -577,3 +577,44 @@ def test_stored_keys_are_what_the_rows_score():
                 assert s[r, pos] == code_val * sc, (r, pos, s[r, pos])
     poisoned = oracle.scores(oracle.Problem(qb, False, w, kc, ks, bt, lens, rreq))
     assert not np.isfinite(poisoned[2, 69:72]).any()
+
+
+def test_prefix_order_worked_example():
+    """The pages' list order, worked by hand.  k = 3 over [1.5000001, 1.0, 1.5,
+    0.5, 0.25, 3.0]: T = 1.5 (image 0xBFC00000).  The keys sharing T's 12-bit
+    prefix 0xBFC are 1.5000001 and 1.5, and they share the 24-bit prefix too.
+    With room >= 2 the radix stops at 12 bits: 3.0 (prefix 0xC04, position 5),
+    then 1.5000001 (prefix 0xBFC, above T, position 0), then the tie at 2.
+    With room 1 it runs to 32 bits: the specification's order, 0, 5, 2."""
+    s = np.array([1.5000001, 1.0, 1.5, 0.5, 0.25, 3.0], np.float32)
+    assert s[0] > s[2]
+    assert oracle.prefix_order(s, 3, 2).tolist() == [5, 0, 2]
+    assert oracle.prefix_order(s, 3, 100).tolist() == [5, 0, 2]
+    assert oracle.prefix_order(s, 3, 1).tolist() == [0, 5, 2]
+    assert oracle.topk(s, 3).tolist() == [0, 5, 2]
+    # a 24-bit stop: 1.5 + 2^-12 shares T's 12-bit prefix but not its 24-bit one
+    s2 = np.array([1.5 + 2.0 ** -12, 1.5000001, 1.5, 0.5, 3.0, 1.0], np.float32)
+    # sorted: 3.0 (4), 1.5+2^-12 (0), 1.5000001 (1), 1.5 (2): k = 4 gives T = 1.5
+    # 12-bit keys: positions 0, 1, 2 (3 keys); 24-bit keys: positions 1, 2 (2 keys)
+    assert oracle.prefix_order(s2, 4, 2).tolist() == [0, 4, 1, 2]   # 24-bit stop: 0 and 4 are above 0xBFC000
+    assert oracle.prefix_order(s2, 4, 3).tolist() == [4, 0, 1, 2]   # 12-bit stop
+    assert oracle.prefix_order(s2, 4, 1).tolist() == [0, 1, 4, 2]   # 32 bits: the specification's order
+    assert oracle.topk(s2, 4).tolist() == [0, 1, 4, 2]
+
+
+def test_prefix_order_properties():
+    """At every stop the list holds oracle_topk's set; room 0 (no prefix can
+    stop: T's own key shares it) gives oracle_topk's list exactly; short rows
+    are oracle_topk's."""
+    rng = np.random.default_rng(21)
+    for trial in range(30):
+        n = int(rng.integers(1, 3000))
+        k = int(rng.integers(1, 400))
+        levels = rng.integers(2, 50)
+        s = (rng.integers(0, levels, n) * rng.choice([1.0, 1.0 / 3.0, 1e-3])).astype(np.float32)
+        s += rng.standard_normal(n).astype(np.float32) * rng.choice([0.0, 1e-6, 1e-2])
+        ref = oracle.topk(s, k)
+        assert np.array_equal(oracle.prefix_order(s, k, 0), ref)
+        for room in (1, 7, 64, 1 << 20):
+            got = oracle.prefix_order(s, k, room)
+            assert sorted(got.tolist()) == sorted(ref.tolist()), (trial, room)
