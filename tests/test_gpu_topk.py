@@ -201,11 +201,12 @@ def test_crowded_first_digit(n, placement, c1):
 
 
 @pytest.mark.parametrize("placement", ["spread", "first_keys"])
-@pytest.mark.parametrize("c1", [4096, 4097])
+@pytest.mark.parametrize("c1", [4096, 4097, 8192, 8193])
 def test_leader_capacity_boundary(placement, c1):
     """A split row whose first digit's threshold bin holds exactly the 4,096
-    candidates the leader slice takes, or one more (then the two further
-    cluster rounds run instead); spread over the row or crowded into its
+    candidates the leader slice takes, or more (then the two further cluster
+    rounds run instead; 8,192 and 8,193 are bins as large as 16 requests x 4
+    rows of random keys produce); spread over the row or crowded into its
     first slices, far from the leader (the last slice)."""
     n = 131072
     rng = np.random.default_rng(c1 + len(placement))
