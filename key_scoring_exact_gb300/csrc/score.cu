@@ -30,7 +30,11 @@
 // key per thread and reduces over heads inside the thread: no cross-lane sums,
 // and each warp stores 32 consecutive scores of a row.
 //
-// One launch, one CTA per SM, persistent over a contiguous range of tiles:
+// Two launches per call:
+//   k_qprep    (small) splits every row's query once into the two E4M3 terms,
+//              laid out as the shared-memory operand (swizzled), and w', in
+//              the workspace; with new keys it first stores them.
+//   k_score    one CTA per SM, persistent over a contiguous range of tiles:
 //   all        build the plan in shared memory: consecutive rows of one
 //              request form groups of at most four rows, each group's keys
 //              are cut into 128-key tiles numbered as work items.
@@ -38,22 +42,27 @@
 //              page per lane), lane 0 issues per tile two key pages (TMA,
 //              128-byte swizzle) + their scales (bulk copy) into stage s of a
 //              7-stage ring.
-//   warp 1     TMEM allocator and MMA issuer: 4 (E4M3 query) or 8 (bf16 query,
-//              hi and lo terms) kind::f8f6f4 MMAs of K = 32 per tile into one
-//              of two TMEM accumulators.
-//   warps 2-17 epilogue.  At each group they first split the group's query
-//              into the swizzled shared-memory operand (while the producer
-//              already streams keys), then per tile one (row, TMEM lane
-//              quadrant) per warp: tcgen05.ld the row's 64 head columns, ReLU,
-//              head-weighted sum (packed f32x2 FMAs), times the key scale,
-//              masked coalesced f32 stores.
+//   warp 1     TMEM allocator and MMA issuer: at each group one bulk copy of
+//              the group's prepared operand and w' into shared memory, then
+//              4 (E4M3 query) or 8 (bf16 query, hi and lo terms)
+//              kind::f8f6f4 MMAs of K = 32 per tile into one of two TMEM
+//              accumulators.
+//   warps 2-17 epilogue, per tile one (row, TMEM lane quadrant) per warp:
+//              tcgen05.ld the row's 64 head columns, ReLU, head-weighted sum
+//              (packed f32x2 FMAs), times the key scale, masked coalesced f32
+//              stores.  Without a prepared operand (the no-allocation entry
+//              point has no room for one) these warps split the group's query
+//              themselves at each group.
 //
-// Every launch is a programmatic dependent of the kernel before it on the
-// stream: its CTAs may start on SMs that kernel frees, set up barriers and
-// TMEM, and wait (griddepcontrol.wait) before touching global memory; each
-// CTA allows the next launch (the selection) once its scores are written.
-// Launches of many tiles per CTA use a second instantiation whose epilogue
-// keeps half of its row's head weights in registers (kRegW below).
+// Launch chaining: k_qprep waits for the kernel before it (griddepcontrol.wait)
+// and then lets k_score launch as its programmatic dependent, so every input
+// written before the call is complete when k_score starts: it builds its plan
+// and starts its key loads at once, and its MMA warp waits for k_qprep's grid
+// before copying an operand.  Without a prepared operand k_score itself waits
+// for the kernel before it before touching global memory.  Each CTA lets the
+// next launch (the selection) start once its scores are written.  Launches
+// of many tiles per CTA use a second instantiation whose epilogue keeps half
+// of its row's head weights in registers (kRegW below).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
