@@ -151,6 +151,31 @@ idx_status idx_score_topk(int qtype, const void *q, const float *head_w,
                           void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * idx_score_topk_ready -- idx_score_topk (same arguments, scores, lists and
+ * errors) for a caller whose block_table, seq_lens, row_req, k_cache and
+ * k_scale are complete when the call is enqueued: written by the host, by
+ * copies or by kernels that have finished, and by no kernel that may still
+ * be running.  q and head_w may still come from the kernel just before the
+ * call on the stream.  The scoring launch then starts on the SMs that kernel
+ * leaves free and builds its plan, reads the block table and fetches its
+ * first key pages while that kernel runs; it reads q and head_w and writes
+ * scores only after that kernel has completed.  In a sequence of decode
+ * steps whose paged-cache metadata is prepared ahead, this overlaps each
+ * step's scoring set-up with the previous step's selection
+ * ("sgl-amd-mono-upstream PR 18", section "Motivation": the indexer launch
+ * is the whole chain, so its fixed latencies are the cost at small sizes).
+ * With inputs that break the condition the scores race with their writer
+ * and are undefined.
+ */
+idx_status idx_score_topk_ready(int qtype, const void *q, const float *head_w,
+                                const uint8_t *k_cache, const float *k_scale, int64_t pool_pages,
+                                const int32_t *block_table, int max_pages,
+                                const int32_t *seq_lens, const int32_t *row_req, int R,
+                                int64_t max_len, int k, int32_t *indices,
+                                float *scores, int64_t score_stride,
+                                void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * idx_score_topk_slots -- idx_score_topk whose lists hold physical cache
  * slots instead of logical positions: a list entry for position p of row r
  * is block_table[row_req[r]][p / IDX_PAGE] * IDX_PAGE + p % IDX_PAGE, the

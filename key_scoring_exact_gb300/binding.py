@@ -23,7 +23,8 @@ STATUS = {0: "IDX_OK", -1: "IDX_ERR_ARG", -2: "IDX_ERR_ALIGN", -3: "IDX_ERR_WORK
 EXPORTS = ("idx_workspace_bytes", "idx_workspace_init", "idx_score", "idx_topk", "idx_score_topk",
            "idx_check_status", "idx_status_str", "idx_version", "idx_score_noalloc",
            "idx_host_workspace_bytes", "idx_score_topk_host", "idx_quantize_query", "idx_score_topk_slots",
-           "idx_score_topk_tagged", "idx_score_topk_newkeys", "idx_score_topk_prefix_order")
+           "idx_score_topk_tagged", "idx_score_topk_newkeys", "idx_score_topk_prefix_order",
+           "idx_score_topk_ready")
 DIAG_EXPORTS = ("idx_probe_fp8_mma", "idx_test_set_wait_limit")   # include/idx_diag.h
 
 _lib = None
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.idx_score_topk.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
     lib.idx_score_topk_slots.restype = i32
     lib.idx_score_topk_slots.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
+    lib.idx_score_topk_ready.restype = i32
+    lib.idx_score_topk_ready.argtypes = score_common + [i64, i32, p, p, i64, p, sz, p]
     lib.idx_score_topk_prefix_order.restype = i32
     lib.idx_score_topk_prefix_order.argtypes = score_common + [i64, i32, i64, p, p, i64, p, sz, p]
     lib.idx_score_topk_newkeys.restype = i32
@@ -211,20 +214,26 @@ def topk(scores, row_lens, k, indices, workspace=None, stream=None):
 
 
 def score_topk(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, indices,
-               workspace, scores=None, stream=None, quantize_q=False, slots=False):
+               workspace, scores=None, stream=None, quantize_q=False, slots=False, inputs_ready=False):
     """idx_score_topk: scoring then selection on one stream.  With scores=None
     the scores live in the workspace (size it with with_scores=True).
     quantize_q: score the on-device FP8 quantisation of a bf16 query.
-    slots: the lists hold physical cache slots (idx_score_topk_slots)."""
+    slots: the lists hold physical cache slots (idx_score_topk_slots).
+    inputs_ready: idx_score_topk_ready -- the block table, lengths, row map,
+    key cache and scales are complete when the call is enqueued (no running
+    kernel writes them), so the scoring's set-up overlaps the kernel before."""
+    if slots and inputs_ready:
+        raise ValueError("slots and inputs_ready are separate entry points")
     args = _score_common(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, quantize_q)
     if indices.shape != (q.shape[0], k):
         raise ValueError("indices must be [R, k]")
     sp = _dev(scores, "scores", torch.float32) if scores is not None else None
     stride = int(scores.shape[1]) if scores is not None else 0
-    fn = load().idx_score_topk_slots if slots else load().idx_score_topk
-    st = fn(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
-            stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
-    _check(st, "idx_score_topk_slots" if slots else "idx_score_topk")
+    name = "idx_score_topk_slots" if slots else ("idx_score_topk_ready" if inputs_ready else "idx_score_topk")
+    st = getattr(load(), name)(*args, int(max_len), int(k), _dev(indices, "indices", torch.int32), sp,
+                               stride, _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                               _stream(stream))
+    _check(st, name)
 
 
 def score_topk_tagged(q, head_w, k_cache, k_scale, block_table, seq_lens, row_req, max_len, k, tag, pairs,

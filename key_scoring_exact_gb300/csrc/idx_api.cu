@@ -224,7 +224,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
                           size_t ws_bytes, void* stream, bool slots, long long* pairs = nullptr,
                           uint32_t tag = 0, const uint8_t* new_k = nullptr, const float* new_scale = nullptr,
-                          int64_t prefix_room = -1) {
+                          int64_t prefix_room = -1, bool inputs_ready = false) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
@@ -251,6 +251,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                 R, scores, score_stride, max_len, ws, L, s, dev.num_sms};
     a.new_k = new_k;
     a.new_scale = new_scale;
+    a.inputs_ready = inputs_ready;
     st = run_score(a);
     if (st != IDX_OK) return st;
     // Each row's selection covers the keys its scores were written for.
@@ -328,6 +329,16 @@ idx_status idx_score_topk(int qtype, const void* q, const float* head_w, const u
                           size_t ws_bytes, void* stream) {
     return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
                            R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false);
+}
+
+idx_status idx_score_topk_ready(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,
+                                const float* k_scale, int64_t pool_pages, const int32_t* block_table,
+                                int max_pages, const int32_t* seq_lens, const int32_t* row_req, int R,
+                                int64_t max_len, int k, int32_t* indices, float* scores, int64_t score_stride,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    return score_topk_impl(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages, seq_lens, row_req,
+                           R, max_len, k, indices, scores, score_stride, workspace, ws_bytes, stream, false,
+                           nullptr, 0, nullptr, nullptr, -1, true);
 }
 
 idx_status idx_score_topk_slots(int qtype, const void* q, const float* head_w, const uint8_t* k_cache,

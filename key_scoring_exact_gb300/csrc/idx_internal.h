@@ -77,6 +77,12 @@ struct ScoreArgs {
     // pointers above are then written.
     const uint8_t* new_k = nullptr;
     const float* new_scale = nullptr;
+    // The caller guarantees that the block table, lengths, row map, key cache
+    // and scales are complete when the call is enqueued (no kernel that may
+    // still be running writes them): the scoring may then launch before
+    // k_qprep's grid wait and read them while the kernel before the call
+    // still runs.
+    bool inputs_ready = false;
 };
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);

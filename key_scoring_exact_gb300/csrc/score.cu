@@ -124,6 +124,7 @@ struct ScoreParams {
     const float* new_scale;
     uint8_t* k_cache_w;      // the cache, written by that store
     float* k_scale_w;
+    int inputs_ready;        // k_qprep lets the scoring launch before its own grid wait
     uint64_t wait_ns;        // wall-time limit of every role's waits (kWaitTimeoutNs in normal use)
     int drop_query_handoff;  // test only: the epilogue never signals the query operand
 };
@@ -374,9 +375,16 @@ __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
     // Wait for the kernel before this one, then let the scoring launch (a
     // programmatic dependent) start: every input written before this call is
     // then complete, so the scoring may read the inputs other than this
-    // kernel's operands before its own grid wait.
+    // kernel's operands before its own grid wait.  When the caller guarantees
+    // that those inputs (block table, lengths, row map, key cache and scales)
+    // were complete when the call was enqueued, the scoring may launch at
+    // once, so that its set-up, plan and first key pages overlap the kernel
+    // before this one; the query and head weights, which that kernel may
+    // still be writing, are read here only after the wait, and the scoring
+    // writes no score before this grid has completed.
+    if (p.inputs_ready) pdl_launch_dependents();
     pdl_wait();
-    pdl_launch_dependents();
+    if (!p.inputs_ready) pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warp_g = blockIdx.x * (kQprepThreads / 32) + (threadIdx.x >> 5);
     const int pairs = p.R * kHeads;
@@ -516,7 +524,8 @@ k_score(const __grid_constant__ CUtensorMap keys_map, const ScoreParams p) {
     }
     // Launched as a programmatic dependent of the kernel before it on the
     // stream.  With a prepared operand that kernel is k_qprep, which lets this
-    // grid launch only once every kernel before it has completed: the plan
+    // grid launch only once every kernel before it has completed (or at once,
+    // when the caller guarantees those inputs complete at enqueue): the plan
     // inputs, block table and keys are read at once (through L2), and the
     // MMA warp waits for k_qprep to finish (griddepcontrol.wait) before
     // copying the operand.  Without one, wait for the kernel before before
@@ -832,6 +841,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.status = reinterpret_cast<uint32_t*>(a.ws + a.L.status);
     p.qop = a.L.qop ? reinterpret_cast<uint8_t*>(a.ws + a.L.qop) : nullptr;
     if (a.new_k && !p.qop) return cudaErrorInvalidValue;  // the store is k_qprep's
+    p.inputs_ready = a.inputs_ready && p.qop ? 1 : 0;
     p.new_k = a.new_k;
     p.new_scale = a.new_scale;
     p.k_cache_w = const_cast<uint8_t*>(a.k_cache);
@@ -848,10 +858,11 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     cfg.blockDim = dim3(kScoreThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = a.stream;
-    // A programmatic dependent of the kernel before it on the stream: its CTAs
-    // may launch (on SMs that kernel leaves free) once that kernel allows it,
-    // and wait for it to finish (griddepcontrol.wait) before touching global
-    // memory.  The selection allows it at its start, the host call's gather
+    // Every launch is a programmatic dependent of the kernel before it on the
+    // stream: its CTAs may launch (on SMs that kernel leaves free) once that
+    // kernel allows it.  k_qprep and, without a prepared operand, k_score wait
+    // for it (griddepcontrol.wait) before reading an input it may write; the
+    // selection allows its dependent at its start, the host call's gather
     // kernel too; any other kernel before it simply completes first.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
