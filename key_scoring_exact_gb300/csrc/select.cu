@@ -142,6 +142,7 @@ struct __align__(16) Shared {
     uint32_t eqc[kMaxCluster];           // leader: candidates equal to T, per slice
     uint32_t ncand;                      // leader: candidates received
     uint32_t lead[4];                    // from the leader: T, kr, keys above / at T before this slice
+    uint32_t bin_min, bin_max;           // one-CTA rows: least and largest key in the first digit's bin
 };
 
 // Exclusive prefix sum over the block in thread order; *total gets the sum.
@@ -185,7 +186,7 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
                                          uint32_t mask, int shift, int nb, uint32_t kr, bool single, int r,
                                          int nslices, bool have_hist, Shared& S, bool last = false,
                                          uint32_t c = 0, int j0 = 0, int j1 = 0, uint32_t* above_out = nullptr,
-                                         uint32_t* cmask_out = nullptr) {
+                                         uint32_t* cmask_out = nullptr, bool tie_check = false) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (!have_hist && last) {
         for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
@@ -216,6 +217,40 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
         *cmask_out = cm;
         above = __reduce_add_sync(kFull, above);
         if (lane == 0 && above) atomicAdd(&S.above, above);
+    } else if (!have_hist && tie_check) {
+        // As the branch below, over the thread's own run; besides the
+        // histogram it marks the keys under the prefix, counts those above it
+        // and finds their least and largest key (S.bin_min, S.bin_max).
+        for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
+        __syncthreads();
+        const uint32_t dm = (uint32_t)nb - 1;
+        uint32_t above = 0, cm = 0, lo = 0xFFFFFFFFu, hi_key = 0u;
+        for (int j = j0; j < j1; ++j) {
+            const uint4 u = reinterpret_cast<const uint4*>(keys)[j];
+            const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (4 * j + q < cnt) {
+                    const uint32_t hi = uu[q] & mask;
+                    if (hi == prefix) {
+                        atomicAdd(&S.hloc[(uu[q] >> shift) & dm], 1u);
+                        cm |= 1u << (4 * (j - j0) + q);
+                        lo = min(lo, uu[q]);
+                        hi_key = max(hi_key, uu[q]);
+                    } else {
+                        above += (uint32_t)(hi > prefix);
+                    }
+                }
+            }
+        }
+        *above_out = above;
+        *cmask_out = cm;
+        lo = __reduce_min_sync(kFull, lo);
+        hi_key = __reduce_max_sync(kFull, hi_key);
+        if (lane == 0) {
+            atomicMin(&S.bin_min, lo);
+            atomicMax(&S.bin_max, hi_key);
+        }
     } else if (!have_hist) {
         for (int b = tid; b < nb; b += kThreads) S.hloc[b] = 0;
         __syncthreads();
@@ -232,6 +267,8 @@ __device__ __forceinline__ void digit_round(const uint32_t* __restrict__ keys, i
         }
     }
     __syncthreads();
+    // every key under the prefix is the same: the caller has T, no scan needed
+    if (tie_check && S.bin_min == S.bin_max) return;
     // Scan in descending digit order: thread tid < nb / bpt holds the bpt
     // digits b0 .. b0 + bpt - 1 (tv[q] = digit b0 + q), b0 = nb - bpt (tid + 1),
     // so threads in order cover the digits from the largest down; others none.
@@ -453,7 +490,11 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         S.gtc[tid] = 0;
         S.eqc[tid] = 0;
     }
-    if (tid == 0) S.ncand = 0;
+    if (tid == 0) {
+        S.ncand = 0;
+        S.bin_min = 0xFFFFFFFFu;
+        S.bin_max = 0u;
+    }
     // This launch is itself a programmatic dependent of the kernel before it
     // (the scoring): wait for that grid before reading a score.
     pdl_wait();
@@ -491,7 +532,7 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
             for (int j = tid; j < k; j += kThreads) put_entry(dst, pdst, sm.tag, j, j < n ? list_entry(page_row, j) : -1);
         return;
     }
-    const bool single = n <= slice_cap;
+    const bool single = CL == 1 || n <= slice_cap;  // one CTA a row: always (rows are cut to its slice above)
     if (single && c != 0) return;   // one CTA serves the row; no cluster barrier is used
     const int cnt = (int)(start < n ? (n - start < slice_cap ? n - start : slice_cap) : 0);
 
@@ -649,15 +690,27 @@ k_select(const float* __restrict__ scores, int64_t len_cap, const int32_t* __res
         base_eq = S.lead[3];
         gt_total = (uint32_t)k - kr;
     } else {
-        // ---- two more cluster rounds (bits 20..10, then 9..0)
-        digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, CL, false, S);
-        prefix |= S.pick[0] << 10;
-        mask |= 0x7FFu << 10;
-        kr -= S.pick[1];
-        digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, false, S, true, c, j0, j1, &above, &cmask);
-        d_last = S.pick[0];
-        T = prefix | d_last;  // the k-th largest radix key of the row
-        kr -= S.pick[1];
+        // ---- two more cluster rounds (bits 20..10, then 9..0).  In a launch of
+        //      one CTA a row, the first of them also checks whether every key in
+        //      the first digit's threshold bin is the same (a tie-heavy row: many
+        //      keys of one value); then T is that key, the pass has marked the
+        //      bin's keys and counted those above it, and the last round is not
+        //      needed.
+        constexpr bool kTieCheck = CL == 1;  // rows on one CTA each (launches of short rows)
+        digit_round(keys_s, cnt, prefix, mask, 10, 2048, kr, single, 1, CL, false, S, false, c, j0, j1, &above,
+                    &cmask, kTieCheck);
+        if (kTieCheck && S.bin_min == S.bin_max) {
+            T = S.bin_min;  // kr of the bin's keys, all equal to T, complete the list
+        } else {
+            prefix |= S.pick[0] << 10;
+            mask |= 0x7FFu << 10;
+            kr -= S.pick[1];
+            digit_round(keys_s, cnt, prefix, mask, 0, 1024, kr, single, 2, CL, false, S, true, c, j0, j1, &above,
+                        &cmask);
+            d_last = S.pick[0];
+            T = prefix | d_last;  // the k-th largest radix key of the row
+            kr -= S.pick[1];
+        }
         gt_total = (uint32_t)k - kr;
     }
 

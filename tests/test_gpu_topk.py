@@ -249,3 +249,61 @@ def test_row_count_and_length_mixes(R, n):
     got, st = gpu_topk(s, lens, 2048)
     assert st == 0
     _check_rows(s, lens, 2048, got)
+
+
+def _bin_row(n, n_bin, values, n_above, seed):
+    """A row of n keys: n_above keys well above, n_bin keys in one first-digit
+    bin ([1.0, 1.25): the top 11 bits of the radix image agree) taking the
+    given values in turn, the rest far below."""
+    rng = np.random.default_rng(seed)
+    s = rng.uniform(0.01, 0.1, n).astype(np.float32)
+    pos = rng.permutation(n)
+    s[pos[:n_above]] = rng.uniform(4.0, 8.0, n_above).astype(np.float32)
+    vals = np.asarray(values, dtype=np.float32)
+    s[pos[n_above:n_above + n_bin]] = vals[np.arange(n_bin) % vals.size]
+    return s
+
+
+@pytest.mark.parametrize("n,n_bin,n_above", [(8192, 2048, 0), (8192, 2048, 1000), (8189, 2047, 2047),
+                                             (12288, 5000, 10), (8192, 511, 1700), (8192, 512, 1700),
+                                             (4000, 3000, 0)])
+def test_one_cta_bin_of_equal_keys(n, n_bin, n_above):
+    """Rows on one CTA whose first digit's threshold bin holds only equal keys
+    (as in the tie cache): T is that key, found without the two lower digit
+    rounds when the bin holds at least 512 keys; the lists are the oracle's,
+    whether the bin's keys all make the list or only some of them."""
+    s = _bin_row(n, n_bin, [1.125], n_above, n + n_bin + n_above)[None, :]
+    got, st = gpu_topk(s, [n], 2048)
+    assert st == 0
+    _check_rows(s, [n], 2048, got)
+
+
+@pytest.mark.parametrize("values", [[1.125, 1.0625], [1.125, np.nextafter(np.float32(1.125), np.float32(2))],
+                                    [1.0, 1.1, 1.2, 1.24]])
+@pytest.mark.parametrize("n_above", [0, 1500])
+def test_one_cta_crowded_bin_of_several_values(values, n_above):
+    """A crowded threshold bin on one CTA whose keys are not all equal (two
+    values one ulp apart among them): the check finds them unequal and the
+    two lower digit rounds pick T; the lists are the oracle's."""
+    n = 8192
+    s = _bin_row(n, 3000, values, n_above, 7 + n_above + len(values))[None, :]
+    got, st = gpu_topk(s, [n], 2048)
+    assert st == 0
+    _check_rows(s, [n], 2048, got)
+
+
+def test_short_tied_row_beside_split_rows():
+    """A tie-cache-like row short enough to run on one CTA of a cluster launch
+    (its other slices leave at once), beside rows split over the cluster."""
+    rows, lens = [], [8192, 131072, 9000, 60000]
+    width = max(lens)
+    for i, n in enumerate(lens):
+        if n <= 9000:
+            r = _bin_row(n, 2500, [1.125], 300 * i, 40 + i)
+        else:
+            r = np.random.default_rng(50 + i).standard_normal(n).astype(np.float32)
+        rows.append(np.pad(r, (0, width - n)))
+    s = np.stack(rows)
+    got, st = gpu_topk(s, lens, 2048)
+    assert st == 0
+    _check_rows(s, lens, 2048, got)
