@@ -144,6 +144,9 @@ struct __align__(16) Shared {
     uint32_t lead[4];                    // from the leader: T, kr, keys above / at T before this slice
     uint32_t bin_min, bin_max;           // one-CTA rows: least and largest key in the first digit's bin
 };
+// 16-byte vector reads of the histograms, local and remote
+static_assert(offsetof(Shared, hloc) % 16 == 0 && offsetof(Shared, htot) % 16 == 0 &&
+                  (kBinsMax * sizeof(uint32_t)) % 16 == 0, "histograms need 16-byte alignment");
 
 // Exclusive prefix sum over the block in thread order; *total gets the sum.
 // Ends with a barrier, so S.wsum may be reused right after.
