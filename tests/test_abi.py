@@ -149,3 +149,28 @@ def test_tagged_and_newkeys_argument_errors_need_no_gpu(lib):
     bad_type = list(base)
     bad_type[0] = 9
     assert lib.idx_score_topk_newkeys(*bad_type, fake, fake, 256, 16, fake, None, 0, fake, 1 << 30, None) == -1
+
+
+def test_ready_entry_point_argument_errors_need_no_gpu(lib):
+    """idx_score_topk_ready takes idx_score_topk's arguments and refuses the
+    same errors before anything is launched: no output, k out of range, a
+    misaligned key cache, a bad query type (the workspace size is checked after
+    the device query, as in idx_score_topk)."""
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    common = [i32, p, p, p, p, i64, p, i32, p, p, i32]
+    lib.idx_score_topk_ready.restype = i32
+    lib.idx_score_topk_ready.argtypes = common + [i64, i32, p, p, i64, p, sz, p]
+    fake = ctypes.c_void_p(1 << 20)
+    base = [0, fake, fake, fake, fake, 8, fake, 4, fake, fake, 2]
+
+    def call(b=base, max_len=256, k=16, idx=fake, ws_bytes=1 << 30):
+        return lib.idx_score_topk_ready(*b, max_len, k, idx, None, 0, fake, ws_bytes, None)
+
+    assert call(idx=None) == -1                          # no output
+    assert call(k=0) == -1 and call(k=4096) == -1        # k outside [1, 2048]
+    bad_cache = list(base)
+    bad_cache[3] = ctypes.c_void_p((1 << 20) + 1)
+    assert call(b=bad_cache) == -2                       # key cache not 16-byte aligned
+    bad_type = list(base)
+    bad_type[0] = 9
+    assert call(b=bad_type) == -1                        # query type
