@@ -5,7 +5,8 @@ tests check every way that overlap could go wrong: scores and lists against
 the oracle on configurations 1-4; calls back to back on one stream with the
 scores in one shared workspace, each scoring starting while the previous
 selection still reads that workspace; a query written by the kernel just
-before the call (allowed by the contract); ready and plain calls mixed."""
+before the call (allowed by the contract); ready and plain calls mixed; two
+and sixteen row groups."""
 import numpy as np
 import pytest
 import torch
@@ -132,3 +133,48 @@ def test_ready_and_plain_calls_mixed():
     assert binding.check_status(ws, stream) == 0
     for i, idx in enumerate(outs):
         assert np.array_equal(idx.cpu().numpy(), ref), "call %d" % i
+
+
+def test_ready_chain_of_eight_rows():
+    """Two row groups of one request through idx_score_topk_ready: every
+    score within 1e-4 of the oracle, every list exact."""
+    w = W.make_extra("chain8")
+    t = device_inputs(w)
+    scores = torch.zeros(w.R, stride_for(w.max_len), dtype=torch.float32, device="cuda")
+    got = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+    ws = binding.new_workspace(w.R, w.max_len, w.k)
+    _call(w, t, got, ws, scores=scores)
+    assert binding.check_status(ws) == 0
+    s = scores.cpu().numpy()
+    errs = checks.score_errors(s, oracle.scores(problem(w)), w.seq_lens.tolist())
+    assert max(errs) <= checks.SCORE_TOL, errs
+    _lists_exact(w, s, got.cpu().numpy())
+
+
+def test_ready_sixteen_requests():
+    """16 requests x 4 rows x 131K keys (16 row groups, the selection in two
+    waves of clusters) through idx_score_topk_ready, twice back to back on one
+    stream: sampled scores within 1e-4 of the oracle, every list exact and the
+    same in both calls."""
+    w = W.make_config(5)
+    t = device_inputs(w)
+    scores = torch.zeros(w.R, stride_for(w.max_len), dtype=torch.float32, device="cuda")
+    ws = binding.new_workspace(w.R, w.max_len, w.k)
+    stream = torch.cuda.Stream()
+    outs = []
+    for _ in range(2):
+        got = torch.full((w.R, w.k), -7, dtype=torch.int32, device="cuda")
+        _call(w, t, got, ws, scores=scores, stream=stream)
+        outs.append(got)
+    stream.synchronize()
+    assert binding.check_status(ws, stream) == 0
+    s = scores.cpu().numpy()
+    pb = problem(w)
+    rng = np.random.default_rng(5)
+    for r, n in enumerate(w.seq_lens.tolist()):
+        pos = np.unique(np.concatenate([[0, 127, 128, n - 1], rng.integers(0, n, 12),
+                                        np.argsort(-s[r, :n])[:4]])).astype(np.int64)
+        ref = oracle.score_positions(pb, r, pos)
+        assert np.max(np.abs(s[r, pos] - ref)) <= checks.SCORE_TOL * np.max(np.abs(ref)), r
+    _lists_exact(w, s, outs[0].cpu().numpy())
+    assert np.array_equal(outs[0].cpu().numpy(), outs[1].cpu().numpy())
