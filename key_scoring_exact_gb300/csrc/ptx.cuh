@@ -131,6 +131,11 @@ IDX_DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* ba
 // async-proxy reads of them (tensor-core operands, bulk copies).
 IDX_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Bring the line holding `ptr` into L2 (no register result, nothing waits on it).
+IDX_DEVI void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)) : "memory");
+}
+
 IDX_DEVI void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

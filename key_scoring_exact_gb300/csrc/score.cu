@@ -369,6 +369,7 @@ __device__ __noinline__ void split_group_query(const ScoreParams& p, int r0, int
 //   w' [R][64] f32 at qop + 2 * R * 8192.
 // A group of rows r0 .. r0 + nr - 1 is then one contiguous run of each.
 constexpr int kQprepThreads = 256;
+constexpr int kPrefetchMinPages = 256;  // rows of at least 16,384 keys get their block table prefetched
 constexpr int kQprepPairsPerWarp = 1;
 
 __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
@@ -388,6 +389,15 @@ __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
     const int lane = threadIdx.x & 31;
     const int warp_g = blockIdx.x * (kQprepThreads / 32) + (threadIdx.x >> 5);
     const int pairs = p.R * kHeads;
+    // Row warp_g's length and request, for the block-table prefetch below
+    // (plain calls only: with inputs complete at enqueue the scoring reads its
+    // block table while the kernel before this one still runs).
+    const bool pf = warp_g < p.R && !p.inputs_ready;
+    int pf_len = 0, pf_req = -1;
+    if (pf) {
+        pf_len = __ldcg(p.seq_lens + warp_g);
+        pf_req = __ldcg(p.row_req + warp_g);
+    }
     if (p.new_k && warp_g < p.R) {
         // The keys this call writes ("sgl-amd-mono-upstream PR 18", section
         // "Modifications / 2", keys this launch writes): row r's key goes to its
@@ -443,6 +453,19 @@ __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
             *reinterpret_cast<uint32_t*>(hi + off) = raw[b].x;
         }
         if (lane == 0) wq[pp] = w_out;
+    }
+    // The block-table entries of every long row into L2, so that the scoring's
+    // producers (which read them right after building their plan) find them
+    // there: a long row's table is otherwise a DRAM miss by the time the next
+    // call reads it.  Short rows' tables are few lines and stay in L2.
+    if (pf) {
+        const int64_t n = min((int64_t)pf_len, p.len_cap);
+        const int npages = (int)((n + kPage - 1) / kPage);
+        if (npages >= kPrefetchMinPages && pf_req >= 0) {
+            const int32_t* row = p.block_table + (int64_t)pf_req * p.max_pages;
+            for (int e = lane * 32; e < npages; e += 1024) prefetch_l2(row + e);
+            if (lane == 0) prefetch_l2(row + npages - 1);
+        }
     }
 }
 
