@@ -224,7 +224,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
                           int32_t* indices, float* scores, int64_t score_stride, void* workspace,
                           size_t ws_bytes, void* stream, bool slots, long long* pairs = nullptr,
                           uint32_t tag = 0, const uint8_t* new_k = nullptr, const float* new_scale = nullptr,
-                          int64_t prefix_room = -1, bool inputs_ready = false) {
+                          int64_t prefix_room = -1, bool inputs_ready = false, bool table_prefetch = true) {
     idx_status st = check_score_args(qtype, q, head_w, k_cache, k_scale, pool_pages, block_table, max_pages,
                                      seq_lens, row_req, R, workspace);
     if (st != IDX_OK) return st;
@@ -252,6 +252,7 @@ static idx_status score_topk_impl(int qtype, const void* q, const float* head_w,
     a.new_k = new_k;
     a.new_scale = new_scale;
     a.inputs_ready = inputs_ready;
+    a.table_prefetch = table_prefetch;
     st = run_score(a);
     if (st != IDX_OK) return st;
     // Each row's selection covers the keys its scores were written for.
@@ -441,11 +442,13 @@ idx_status host_launches(const HostCall& c, cudaStream_t s) {
     // previous call's selection runs, the scoring's CTAs set up while the
     // gather runs; each waits for its predecessor before writing (and the
     // scoring before reading what the gather wrote).
+    // (the gather has just written the block table: it is in L2, no prefetch)
     const idx_status st =
-        idx_score_topk(c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale,
-                       c.pool_pages, reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages,
-                       reinterpret_cast<const int32_t*>(c.ws + H.lens), reinterpret_cast<const int32_t*>(c.ws + H.rreq),
-                       c.R, c.max_len, c.k, c.idx_out, nullptr, 0, c.ws, c.ws_bytes, s);
+        score_topk_impl(c.qtype, c.ws + H.q, reinterpret_cast<const float*>(c.ws + H.w), c.k_cache, c.k_scale,
+                        c.pool_pages, reinterpret_cast<const int32_t*>(c.ws + H.bt), c.max_pages,
+                        reinterpret_cast<const int32_t*>(c.ws + H.lens), reinterpret_cast<const int32_t*>(c.ws + H.rreq),
+                        c.R, c.max_len, c.k, c.idx_out, nullptr, 0, c.ws, c.ws_bytes, s, false, nullptr, 0, nullptr,
+                        nullptr, -1, false, false);
     if (st != IDX_OK) return st;
     int32_t* idx_dev = reinterpret_cast<int32_t*>(c.ws + H.idx);
     if (c.idx_out == idx_dev && cudaMemcpyAsync(c.indices_host, idx_dev, (size_t)c.R * (size_t)c.k * 4,

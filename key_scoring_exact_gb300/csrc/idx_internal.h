@@ -83,6 +83,9 @@ struct ScoreArgs {
     // k_qprep's grid wait and read them while the kernel before the call
     // still runs.
     bool inputs_ready = false;
+    // k_qprep prefetches long rows' block-table entries into L2 (off when the
+    // table was written just before the call and is in L2 already).
+    bool table_prefetch = true;
 };
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map);

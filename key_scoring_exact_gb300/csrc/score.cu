@@ -125,6 +125,7 @@ struct ScoreParams {
     uint8_t* k_cache_w;      // the cache, written by that store
     float* k_scale_w;
     int inputs_ready;        // k_qprep lets the scoring launch before its own grid wait
+    int table_prefetch;      // k_qprep prefetches long rows' block-table entries into L2
     uint64_t wait_ns;        // wall-time limit of every role's waits (kWaitTimeoutNs in normal use)
     int drop_query_handoff;  // test only: the epilogue never signals the query operand
 };
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kQprepThreads) k_qprep(const ScoreParams p) {
     // Row warp_g's length and request, for the block-table prefetch below
     // (plain calls only: with inputs complete at enqueue the scoring reads its
     // block table while the kernel before this one still runs).
-    const bool pf = warp_g < p.R && !p.inputs_ready;
+    const bool pf = warp_g < p.R && p.table_prefetch;
     int pf_len = 0, pf_req = -1;
     if (pf) {
         pf_len = __ldcg(p.seq_lens + warp_g);
@@ -865,6 +866,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& keys_map) {
     p.qop = a.L.qop ? reinterpret_cast<uint8_t*>(a.ws + a.L.qop) : nullptr;
     if (a.new_k && !p.qop) return cudaErrorInvalidValue;  // the store is k_qprep's
     p.inputs_ready = a.inputs_ready && p.qop ? 1 : 0;
+    p.table_prefetch = a.table_prefetch && !a.inputs_ready ? 1 : 0;
     p.new_k = a.new_k;
     p.new_scale = a.new_scale;
     p.k_cache_w = const_cast<uint8_t*>(a.k_cache);
